@@ -1,0 +1,339 @@
+"""Benchmark of the DeepSeekMoE layer forward on B300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one whole layer forward (router, dispatch, gate-up GEMM with
+SwiGLU, down GEMM with the gate-weighted scatter-add, cast) over one batch of
+T synthetic tokens, inputs resident in HBM. Default workload: the
+DeepSeekMoE-16B-shaped layer at T = 16384 tokens. With N > 1 (torchrun) every
+rank runs an independent replica on its own GPU (the layer's tokens are
+independent; no collective is on the data path): weak scaling.
+
+Prints one JSON line (rank 0). `value` is whole-job tokens/s (all ranks'
+tokens / max-over-ranks time); `e2e` is the same metric through the public
+API with the step's x copied in from pinned host memory and y copied back
+inside the timed region; `roofline` is the gate-up GEMM (the dominant kernel)
+measured live with CUDA events recorded inside the library call on the
+stream the kernels run on; `cpu_baseline` is the fp64 CPU oracle timed on a
+bounded sample of the same workload.
+
+--impl reference times that oracle itself, as it stands, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_91_b300 import inputs, workloads  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s & TFLOP/s at 1 B300; % dense-BF16 roofline"
+L2_BYTES = 126 * 2**20
+
+
+def peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_flops(w) -> dict:
+    """Algorithmic FLOPs per launch of each kernel (expected rows from routing:
+    T*k routed + K_s*T shared; every row does d x I products)."""
+    rows = w.T * w.top_k + w.n_shared * w.T
+    return {"router": 2.0 * w.T * w.d * w.n_routed * (2 if w.noisy else 1),
+            "gate_up": 4.0 * rows * w.d * w.d_ff,
+            "down": 2.0 * rows * w.d * w.d_ff}
+
+
+def algorithmic_bytes(w, touched_experts: int) -> float:
+    """Touched expert weights + W_g (+ W_noise) + x + y (+ eps): the method's own traffic."""
+    act = 4 if w.fp32 else 2
+    wts = touched_experts * 3 * w.d * w.d_ff * act
+    router = w.d * w.n_routed * 4 * (2 if w.noisy else 1)
+    xy = 2 * w.T * w.d * act
+    eps = w.T * w.n_routed * 4 if w.noisy else 0
+    return float(wts + router + xy + eps)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def ncu_traffic(kernel_src: str) -> dict | None:
+    """DRAM bytes per launch of the gate-up kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "gate_up_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    return rec if rec.get("source_sha") == sha else None
+
+
+def cpu_oracle_rate(w, inp, budget_s: float) -> dict:
+    """The fp64 oracle (route + sparse SwiGLU experts) on a bounded token sample."""
+    from oracle import moe_oracle as O
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:  # noqa: BLE001
+        cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+
+    def run(n):
+        toks = np.sort(rng.choice(w.T, n, replace=False))
+        x = inp["x"][torch.from_numpy(toks)]
+        eps = inp["eps"][torch.from_numpy(toks)] if inp["eps"] is not None else None
+        t0 = time.perf_counter()
+        r = O.route(x, inp["W_g"], w.top_k, renormalize=w.renormalize, noisy=w.noisy,
+                    W_noise=inp["W_noise"], eps=eps, bias=inp["bias"])
+        O.moe_forward(x, inp["W1"], inp["W3"], inp["W2"], w.n_shared, r["ids"], r["gates"])
+        return time.perf_counter() - t0
+
+    n = min(64, w.T)
+    dt = run(n)
+    if dt < budget_s / 4 and n < w.T:   # grow the sample toward the time budget
+        n = int(min(w.T, max(n, n * budget_s / max(dt, 1e-3) * 0.8)))
+        dt = run(n)
+    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name}: fp64 route + sparse SwiGLU experts "
+                      f"(numpy/BLAS), {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = inputs.make_inputs(w)
+    budget = 20.0
+    steps = []
+    for _ in range(args.warmup + args.steps):
+        steps.append(cpu_oracle_rate(w, inp, budget / max(1, args.steps + args.warmup)))
+    timed = steps[args.warmup:]
+    val = statistics.median(s["value"] for s in timed)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
+                       "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff},
+            "cpu_baseline": {**timed[-1], "value": val},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=workloads.HEADLINE.name, choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = workloads.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    from mixture_experts_layer_91_b300 import binding
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    inp = inputs.make_inputs(w)
+    layer = binding.MoELayer(w, inp, device=dev)
+    x = inp["x"].to(dev)
+    eps = inp["eps"].to(dev) if inp["eps"] is not None else None
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing, with stage events recorded inside the call
+    for _ in range(args.warmup):
+        layer(x, eps)
+    barrier()
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.PROFILE_EVENTS)]
+               for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        layer.profiled(x, step_ev[i], eps)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    st, raw = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device fault flag {raw} after the timed region")
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = tt.item()
+    ms_step = ms_total / args.steps
+    stage_names = ["router", "dispatch", "gate_up", "down", "cast"]
+    stage_ms = {n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_ev)
+                for j, n in enumerate(stage_names)}
+
+    # ---- end to end through the public API: pinned host x in, host y out
+    x_host = inp["x"].pin_memory()
+    eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
+    y_host = torch.empty(w.T, w.d, dtype=layer.y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    eps_dev = torch.empty_like(eps) if eps is not None else None
+    for _ in range(args.warmup):
+        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
+    barrier()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
+    e_end.record(stream)
+    barrier()
+    ms_e2e = e_start.elapsed_time(e_end) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = tt.item()
+
+    # ---- counts of touched experts for the algorithmic bytes
+    _, _, _, counts = binding.forward(layer.cfg, x, layer.W_g, layer.W_noise, eps, layer.bias,
+                                      layer.W1, layer.W3, layer.W2, workspace=layer.workspace,
+                                      routing=True)
+    touched = int((counts > 0).sum().item()) + w.n_shared
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    pk, pk_kind = peaks()
+    kf = kernel_flops(w)
+    gu_s = stage_ms["gate_up"] / 1e3
+    gu_tflops = kf["gate_up"] / gu_s / 1e12
+    peak = pk["bf16_tflops"]
+    src = os.path.join(ROOT, "mixture_experts_layer_91_b300", "csrc", "gemm_tc.cuh")
+    tr = ncu_traffic(src)
+    flops = w.flops()
+    tokens_per_s = world * w.T / (ms_step / 1e3)
+    tflops = world * flops / (ms_step / 1e3) / 1e12
+    ab = algorithmic_bytes(w, touched)
+    roof_time = max(flops / (pk["bf16_tflops"] * 1e12), ab / (pk["hbm_gbs"] * 1e9))
+    launches_per_step = 7 if not w.fp32 else 6
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.fp32 else "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; no checkpoint)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
+                   "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
+                   "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {ab / 2**20:.0f} MiB of weights+activations per step"},
+        "tflops": tflops,
+        "roofline_fraction_layer": roof_time / (ms_step / 1e3) * world,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_tc<SwiGLU> (gate-up)",
+                     "achieved": gu_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": gu_tflops / peak, "peak_kind": f"{pk_kind} burst bf16",
+                     "frac_of_sustained": gu_tflops / pk.get("bf16_tflops_sustained", peak),
+                     "traffic": tr["traffic_bytes_per_launch"] if tr else None,
+                     "algorithmic_flops_per_launch": kf["gate_up"]},
+        "kernels_ms": stage_ms,
+        "kernels_tflops": {"gate_up": gu_tflops,
+                           "down": kf["down"] / (stage_ms["down"] / 1e3) / 1e12,
+                           "router": kf["router"] / (stage_ms["router"] / 1e3) / 1e12},
+        "e2e": {"value": world * w.T / (ms_e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size()
+                + (eps_host.numel() * 4 if eps_host is not None else 0),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_oracle_rate(w, inp, 12.0)
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

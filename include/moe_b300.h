@@ -1,0 +1,226 @@
+/*
+ * moe_b300.h -- C ABI of the DeepSeekMoE layer forward for one B300 GPU (sm_103a).
+ *
+ * The layer (DeepSeekMoE, Chinese translation on gitcode.csdn.net, section 3.2,
+ * eqs (9)-(11)):
+ *
+ *   s_t   = Softmax(u_t . W_g)                       over the N_r routed experts
+ *   g_t   = s_t on Topk(s_t, k), 0 elsewhere           (optionally renormalised)
+ *   y_t   = sum_{i<K_s} FFN_i(u_t) + sum_{i routed} g_{i,t} FFN_i(u_t)
+ *   FFN_i(u) = W2_i (silu(W1_i u) * (W3_i u))          (SwiGLU expert)
+ *
+ * y_t excludes the residual +u_t of eq (9); the caller adds it. Two gate
+ * variants are supported: the noisy top-k gate of "Outrageously Large Neural
+ * Networks" ("Mixture of Experts" notes on blog.carolineworld.cn, section 2,
+ * Noisy Top-K Gating) and the auxiliary-loss-free per-expert selection bias
+ * ("DeepSeek MoE" article on cloud.tencent.com, load-balancing section).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them after the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). No entry point synchronises the stream except
+ *     moe_device_status().
+ *   - Layouts are row-major and dense. Expert weights are stacked shared
+ *     experts first, then routed (eq (9)'s numbering): routed expert r is
+ *     expert K_s + r. W1, W3: [K_s+N_r, I, d]; W2: [K_s+N_r, d, I].
+ *   - act_dtype selects the element type of x, x_perm, expert weights and y:
+ *     MOE_DT_BF16 (bf16, tensor-core path) or MOE_DT_F32 (fp32 CUDA-core path).
+ *     Router weights, noise, bias, gates and logits are always fp32; index
+ *     arrays are int32.
+ *   - Errors are returned as moe_status; nothing is thrown across the ABI.
+ *     Invalid arguments are rejected on the host before anything is enqueued.
+ *     Faults found on the device (an expert id out of range, a pipeline wait
+ *     that exceeded its time limit) set a sticky per-device flag that
+ *     moe_device_status() reports; the kernels skip the offending access.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer      */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid but outside what the kernels implement    */
+  MOE_ERR_WORKSPACE = 3,      /* workspace smaller than the *_workspace_size()   */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed               */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired (pipeline fault)*/
+  MOE_ERR_DEVICE_INDEX = 6    /* a kernel met an out-of-range expert id          */
+} moe_status;
+
+typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  MOE_GATE_SOFTMAX = 0,       /* s = Softmax(x W_g); key s (+ bias); gate s      */
+  MOE_GATE_NOISY = 1          /* H = x W_g + eps * softplus(x W_noise); key H;
+                                 gate = softmax of H over the kept top-k          */
+} moe_gate;
+
+/* Shape and mode of one MoE layer. Fixed-width fields only (stable ABI). */
+typedef struct {
+  int64_t T;           /* tokens (rows of x), >= 0                               */
+  int32_t d;           /* model width, multiple of 8                             */
+  int32_t n_routed;    /* N_r routed experts, 1..256 (2*N_r <= 256 when noisy)   */
+  int32_t n_shared;    /* K_s shared experts, always active, 0..64               */
+  int32_t top_k;       /* k routed experts per token, 1..min(N_r, 32)            */
+  int32_t d_ff;        /* I, intermediate width of every expert, multiple of 8   */
+  int32_t renormalize; /* 1: gates divided by their sum over the selected set    */
+  int32_t gate;        /* moe_gate                                               */
+  int32_t act_dtype;   /* moe_dtype                                              */
+} moe_config;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+int moe_version(void);
+
+/*
+ * moe_route -- the gate: router GEMM, softmax, top-k and gate values.
+ * DeepSeekMoE translation, section 3.2, eqs (10)-(11); noisy variant per the
+ * Noisy Top-K Gating passage of the "Mixture of Experts" notes, section 2;
+ * bias per the cloud.tencent.com article's auxiliary-loss-free section.
+ *
+ *   x        [T, d]   act_dtype      token activations u_t
+ *   W_g      [d, N_r] fp32           expert centroids as columns
+ *   W_noise  [d, N_r] fp32           noise projection; required iff gate = NOISY
+ *   eps      [T, N_r] fp32           the StandardNormal() draws; iff gate = NOISY
+ *   bias     [N_r]    fp32 or NULL   added to s for selection only (SOFTMAX gate)
+ *   topk_ids [T, k]   int32  (out)   selected routed experts, descending key,
+ *                                    ties to the lowest index
+ *   topk_w   [T, k]   fp32   (out)   gate values g_{i,t} of those experts
+ *   logits   [T, N_r] fp32 or NULL (out) the plain logits x W_g
+ * Arithmetic is fp32 throughout (logits accumulated in fp32 FMA).
+ */
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g,
+                     const float* W_noise, const float* eps, const float* bias,
+                     int32_t* topk_ids, float* topk_w, float* logits, void* stream);
+
+/* Bytes of scratch moe_permute needs (per-block histograms and ranks). */
+size_t moe_permute_workspace_size(const moe_config* cfg);
+
+/*
+ * moe_permute -- token dispatch: group the T*k assignments by expert.
+ * The pages say each token goes to its selected experts (DeepSeekMoE
+ * translation, section 2) and that the gate keeps a running per-expert
+ * counter c_e ("Mixture of Experts" notes, section 3, GShard expert capacity).
+ * Rows of expert e occupy [offsets[e], offsets[e+1]) in ascending flat
+ * assignment index a = t*k + j (stable by token).
+ *
+ *   x         [T, d]       act_dtype   activations
+ *   topk_ids  [T, k]       int32       routed expert of each assignment
+ *   workspace, ws_bytes                scratch, >= moe_permute_workspace_size()
+ *   counts    [N_r]        int32 (out) assignments per expert (c_e)
+ *   offsets   [N_r + 1]    int32 (out) exclusive prefix sum of counts
+ *   dest      [T, k]       int32 (out) grouped row of each assignment
+ *   perm_src  [T*k]        int32 (out) flat assignment index of each grouped row
+ *   x_perm    [T*k, d]     act_dtype (out) x_perm[dest[t,j]] = x[t]
+ * Ids outside [0, N_r) are skipped and raise MOE_ERR_DEVICE_INDEX.
+ */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                       void* workspace, size_t ws_bytes, int32_t* counts, int32_t* offsets,
+                       int32_t* dest, int32_t* perm_src, void* x_perm, void* stream);
+
+/* Bytes of scratch moe_expert_ffn needs (group plan and the SwiGLU activations). */
+size_t moe_expert_ffn_workspace_size(const moe_config* cfg);
+
+/*
+ * moe_expert_ffn -- every active expert FFN on its rows, unweighted.
+ * Expert FFN: W2 (silu(W1 x) * (W3 x)); each expert is a standard FFN
+ * (DeepSeekMoE translation, section 2), evaluated only on the tokens routed
+ * to it (sparse evaluation, "Mixture of Experts" notes, section 2).
+ *
+ *   x         [T, d]        act_dtype  activations (the rows of shared experts)
+ *   x_perm    [T*k, d]      act_dtype  grouped rows from moe_permute
+ *   offsets   [N_r + 1]     int32      group bounds from moe_permute
+ *   W1, W3    [K_s+N_r, I, d] act_dtype; W2 [K_s+N_r, d, I] act_dtype
+ *   workspace, ws_bytes                scratch, >= moe_expert_ffn_workspace_size()
+ *   out_rows  [K_s*T + T*k, d] fp32 (out): row i*T + t = FFN_i(x_t) for shared
+ *             expert i; row K_s*T + r = FFN_{K_s+e}(x_perm[r]) for r in group e.
+ * bf16: tcgen05 tensor-core GEMMs, fp32 accumulation, SwiGLU activations
+ * rounded to bf16 between the two GEMMs. fp32: CUDA-core FMA throughout.
+ */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x, const void* x_perm,
+                          const int32_t* offsets, const void* W1, const void* W3,
+                          const void* W2, void* workspace, size_t ws_bytes,
+                          float* out_rows, void* stream);
+
+/*
+ * moe_combine -- gate-weighted combine back to token order (eq (9) without
+ * the residual; "Mixture of Experts" notes, section 3, y_s = sum_e G_{s,e} FFN_e(x_s)):
+ *   y_t = sum_{i<K_s} out_rows[i*T + t] + sum_j topk_w[t,j] out_rows[K_s*T + dest[t,j]]
+ *   out_rows [K_s*T + T*k, d] fp32; dest [T, k] int32; topk_w [T, k] fp32;
+ *   y [T, d] act_dtype (out). Summed in fp32 in a fixed order (deterministic).
+ */
+moe_status moe_combine(const moe_config* cfg, const float* out_rows, const int32_t* dest,
+                       const float* topk_w, void* y, void* stream);
+
+/* Bytes of scratch moe_forward needs. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/*
+ * moe_forward -- the whole layer: route, dispatch, grouped SwiGLU experts and
+ * the gate-weighted combine, fused as: router -> histogram/scan/plan ->
+ * gather -> gate-up GEMM with SiLU*up fused -> down GEMM whose epilogue
+ * scatter-adds g * FFN into an fp32 accumulator (shared experts at gate 1)
+ * -> cast to y. Arguments as in moe_route / moe_expert_ffn.
+ *   y            [T, d]  act_dtype (out)
+ *   topk_ids_out [T, k]  int32 or NULL (out) routing decisions
+ *   topk_w_out   [T, k]  fp32  or NULL (out) gate values
+ *   counts_out   [N_r]   int32 or NULL (out) tokens per routed expert
+ * The scatter-add uses fp32 atomics, so the summation order of the k + K_s
+ * contributions to a token (not the result's tolerance) varies run to run.
+ */
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
+                       const float* W_noise, const float* eps, const float* bias,
+                       const void* W1, const void* W3, const void* W2,
+                       void* workspace, size_t ws_bytes, void* y,
+                       int32_t* topk_ids_out, float* topk_w_out, int32_t* counts_out,
+                       void* stream);
+
+/* Number of events moe_forward_profiled records per call. */
+#define MOE_PROFILE_EVENTS 6
+
+/*
+ * moe_forward_profiled -- moe_forward, plus cudaEventRecord of caller-created
+ * events on `stream` at the stage boundaries, so a caller can time each
+ * kernel of the layer on the stream it runs on. stage_events holds
+ * MOE_PROFILE_EVENTS cudaEvent_t handles (or is NULL, which makes the call
+ * identical to moe_forward): [0] before the router, [1] after the router,
+ * [2] after dispatch (count, scan+plan, gather), [3] after the gate-up GEMM,
+ * [4] after the down GEMM with the scatter-add, [5] after the cast to y.
+ */
+moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const float* W_g,
+                                const float* W_noise, const float* eps, const float* bias,
+                                const void* W1, const void* W3, const void* W2,
+                                void* workspace, size_t ws_bytes, void* y,
+                                int32_t* topk_ids_out, float* topk_w_out, int32_t* counts_out,
+                                void* stream, void* const* stage_events);
+
+/*
+ * moe_device_status -- synchronise `stream`, then read and clear the sticky
+ * device fault flag of the current device. Returns MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX or MOE_ERR_CUDA. Writes the
+ * raw flag word to *raw when raw is not NULL.
+ */
+moe_status moe_device_status(void* stream, int32_t* raw);
+
+/*
+ * moe_debug_wait_timeout -- test hook for the bounded-wait machinery: enqueue
+ * one kernel that waits on an mbarrier nothing ever arrives on, with a limit
+ * of `limit_us` microseconds (1..2000000). The wait runs out, the kernel sets
+ * the MOE_ERR_DEVICE_TIMEOUT flag and returns; the context stays usable.
+ */
+moe_status moe_debug_wait_timeout(uint32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,274 @@
+// dispatch.cuh -- grouping the T*k assignments by expert, the group plan of
+// the grouped GEMMs, and the token-order combine.
+//
+// The gate keeps a running per-expert counter c_e of assigned tokens
+// ("Mixture of Experts" notes on blog.carolineworld.cn, section 3, GShard
+// expert capacity); here the counters become a stable counting sort:
+//   count_kernel   per block of 1024 assignments: per-expert counts and the
+//                  rank of every assignment among earlier ones of its expert
+//                  (warp match_any + popc, stable in flat index t*k + j);
+//   scan_kernel    one CTA: per-expert totals, offsets (exclusive scan),
+//                  per-block bases, and the GEMM group plan;
+//   scatter_kernel dest / perm_src and the row gather x -> x_perm (16-byte
+//                  vectors, one warp per assignment).
+// combine_kernel is the gate-weighted sum back to token order (DeepSeekMoE
+// translation, section 3.2, eq (9), without the residual).
+#pragma once
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+
+namespace moe {
+
+constexpr int kCountBlock = 1024;        // assignments per count block
+constexpr int kCountThreads = 256;       // 8 warps x 128 assignments
+constexpr int kCountPerWarp = kCountBlock / (kCountThreads / 32);
+
+__global__ void __launch_bounds__(kCountThreads)
+    count_kernel(const int32_t* __restrict__ ids, int64_t n, int32_t E,
+                 int32_t* __restrict__ blk_hist, int32_t* __restrict__ local_rank) {
+  extern __shared__ int32_t wh[];   // [8][E] per-warp counts
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 8 * E; i += kCountThreads) wh[i] = 0;
+  __syncthreads();
+
+  const int64_t wbase = static_cast<int64_t>(blockIdx.x) * kCountBlock + warp * kCountPerWarp;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int32_t ev[kCountPerWarp / 32];
+  int32_t rk[kCountPerWarp / 32];
+#pragma unroll
+  for (int c = 0; c < kCountPerWarp / 32; ++c) {
+    const int64_t a = wbase + c * 32 + lane;
+    int32_t e = -1;
+    if (a < n) {
+      e = __ldg(ids + a);
+      if (e < 0 || e >= E) {
+        raise_fault(kFaultIndex);
+        e = -1;
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int32_t prev = 0;
+    if (e >= 0) prev = wh[warp * E + e];
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wh[warp * E + e] = prev + __popc(peers);
+    __syncwarp();
+    ev[c] = e;
+    rk[c] = prev + __popc(peers & lt_mask);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kCountThreads) {
+    int32_t run = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int32_t v = wh[w * E + e];
+      wh[w * E + e] = run;
+      run += v;
+    }
+    blk_hist[static_cast<int64_t>(blockIdx.x) * E + e] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kCountPerWarp / 32; ++c) {
+    const int64_t a = wbase + c * 32 + lane;
+    if (a < n && ev[c] >= 0) local_rank[a] = rk[c] + wh[warp * E + ev[c]];
+  }
+}
+
+struct PlanOut {
+  int32_t* mt_start;  // [G+1]
+  int32_t* gsize;     // [G]
+  int32_t* a_row;     // [G]
+  int32_t* o_row;     // [G]
+};
+
+// Group plan from per-expert offsets (one CTA; called by scan_kernel and
+// plan_kernel). Groups: K_s shared (all T tokens, A rows from x), then N_r
+// routed (A rows from x_perm at offsets[e]). Unpadded per-row output: shared
+// group i at rows i*T, routed group e at K_s*T + offsets[e]. m-tiles are 128
+// rows; the padded H row of a group is 128 * mt_start[g].
+__device__ void plan_groups(const int32_t* offsets, int32_t E, int32_t K_s, int64_t T,
+                            const PlanOut& o, int32_t* s_tiles /* smem [G] */) {
+  const int32_t G = K_s + E;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    int32_t size, arow;
+    int64_t orow;
+    if (g < K_s) {
+      size = static_cast<int32_t>(T);
+      arow = 0;
+      orow = static_cast<int64_t>(g) * T;
+    } else {
+      const int e = g - K_s;
+      arow = offsets[e];
+      size = offsets[e + 1] - arow;
+      orow = static_cast<int64_t>(K_s) * T + arow;
+    }
+    o.gsize[g] = size;
+    o.a_row[g] = arow;
+    o.o_row[g] = static_cast<int32_t>(orow);
+    s_tiles[g] = (size + kTcBM - 1) / kTcBM;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t run = 0;
+    for (int g = 0; g < G; ++g) {
+      o.mt_start[g] = run;
+      run += s_tiles[g];
+    }
+    o.mt_start[G] = run;
+  }
+  __syncthreads();
+}
+
+constexpr int kScanThreads = 1024;
+
+// One CTA. blk_hist [nblk][E]: per-block counts in, per-block bases out
+// (offsets[e] + counts of expert e in earlier blocks).
+__global__ void __launch_bounds__(kScanThreads)
+    scan_kernel(int32_t* __restrict__ blk_hist, int32_t nblk, int32_t E, int32_t* __restrict__ counts,
+                int32_t* __restrict__ offsets, int32_t K_s, int64_t T, PlanOut plan, int32_t with_plan) {
+  __shared__ int32_t tot[kMaxGroups + 1];
+  __shared__ int32_t part[kScanThreads];
+  // split the block range of each expert over `parts` threads
+  const int parts = max(1, kScanThreads / E);
+  const int e = threadIdx.x % E;
+  const int pi = threadIdx.x / E;
+  const bool active = pi < parts && threadIdx.x < parts * E;
+  const int span = (nblk + parts - 1) / parts;
+  const int b0 = pi * span, b1 = min(nblk, b0 + span);
+  int32_t run = 0;
+  if (active)
+    for (int b = b0; b < b1; ++b) run += blk_hist[static_cast<int64_t>(b) * E + e];
+  part[threadIdx.x] = active ? run : 0;
+  __syncthreads();
+  if (threadIdx.x < E) {
+    int32_t s = 0;
+    for (int j = 0; j < parts; ++j) s += part[j * E + threadIdx.x];
+    tot[threadIdx.x] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t r = 0;
+    for (int i = 0; i < E; ++i) {
+      const int32_t c = tot[i];
+      counts[i] = c;
+      offsets[i] = r;
+      tot[i] = r;
+      r += c;
+    }
+    offsets[E] = r;
+  }
+  __syncthreads();
+  if (active) {
+    int32_t base = tot[e];
+    for (int j = 0; j < pi; ++j) base += part[j * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const int64_t i = static_cast<int64_t>(b) * E + e;
+      const int32_t v = blk_hist[i];
+      blk_hist[i] = base;
+      base += v;
+    }
+  }
+  if (with_plan) {
+    __syncthreads();
+    __shared__ int32_t s_tiles[kMaxGroups];
+    plan_groups(offsets, E, K_s, T, plan, s_tiles);
+  }
+}
+
+// Plan from caller-supplied offsets (the moe_expert_ffn stage entry point).
+__global__ void plan_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t K_s, int64_t T,
+                            PlanOut plan) {
+  __shared__ int32_t s_tiles[kMaxGroups];
+  plan_groups(offsets, E, K_s, T, plan, s_tiles);
+}
+
+// dest / perm_src and the row gather. One warp per assignment, grid-stride.
+template <typename TX>
+__global__ void __launch_bounds__(256)
+    scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int32_t k, int32_t E,
+                   const int32_t* __restrict__ blk_base, const int32_t* __restrict__ local_rank,
+                   const TX* __restrict__ x, int32_t d, int32_t* __restrict__ dest,
+                   int32_t* __restrict__ perm_src, TX* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t nvec = static_cast<int64_t>(d) * sizeof(TX) / 16;
+  for (int64_t a = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; a < n;
+       a += nwarps) {
+    const int32_t e = __ldg(ids + a);
+    if (e < 0 || e >= E) {   // counted as a fault by count_kernel
+      if (lane == 0) dest[a] = -1;
+      continue;
+    }
+    const int32_t r = __ldg(blk_base + (a / kCountBlock) * E + e) + __ldg(local_rank + a);
+    if (lane == 0) {
+      dest[a] = r;
+      perm_src[r] = static_cast<int32_t>(a);
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (a / k) * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(r) * d);
+    for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+// y_t = sum_{i<K_s} rows[i*T + t] + sum_j w[t,j] rows[K_s*T + dest[t,j]]; one
+// CTA per token, fixed summation order.
+template <typename TY>
+__global__ void __launch_bounds__(256)
+    combine_kernel(const float* __restrict__ rows, const int32_t* __restrict__ dest,
+                   const float* __restrict__ w, int64_t T, int32_t d, int32_t k, int32_t K_s,
+                   TY* __restrict__ y) {
+  const int64_t t = blockIdx.x;
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < K_s; ++i) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(rows + (i * T + t) * d + c));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    for (int j = 0; j < k; ++j) {
+      const int32_t r = __ldg(dest + t * k + j);
+      if (r < 0) continue;
+      const float g = __ldg(w + t * k + j);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(rows + (K_s * T + r) * d + c));
+      acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
+    }
+    TY* out = y + t * d + c;
+    out[0] = from_f32<TY>(acc.x);
+    out[1] = from_f32<TY>(acc.y);
+    out[2] = from_f32<TY>(acc.z);
+    out[3] = from_f32<TY>(acc.w);
+  }
+}
+
+// fp32 accumulator -> bf16 output, 8 elements per thread per step.
+__global__ void __launch_bounds__(256)
+    cast_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n8) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(src) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 2 * i + 1);
+    uint4 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4*>(dst)[i] = o;
+  }
+}
+
+// Test hook: a wait on an mbarrier that nothing arrives on, bounded by limit_ns.
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort;
+  if (threadIdx.x == 0) {
+    abort = 0;
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_addr(&bar), 0, &abort, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace moe

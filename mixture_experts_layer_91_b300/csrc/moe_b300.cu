@@ -1,0 +1,581 @@
+// moe_b300.cu -- the C ABI of the DeepSeekMoE layer forward (include/moe_b300.h).
+//
+// One translation unit: the kernels live in the included headers, so the
+// sticky device fault flag is a single static __device__ word.
+//
+// Host side: argument validation (nothing is enqueued on a bad argument),
+// workspace carving (the caller owns all memory; the library allocates
+// nothing), TMA tensor-map encoding per call, and the launches, all
+// asynchronous on the caller's stream.
+
+#include <algorithm>
+#include <functional>
+#include <mutex>
+
+#include "../../include/moe_b300.h"
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "gemm_simt.cuh"
+#include "gemm_tc.cuh"
+#include "router.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kVersion = (1 << 16) | 0;
+constexpr int kMaxDevices = 64;
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_config(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d <= 0 || c->d_ff <= 0 || c->n_routed < 1 || c->n_shared < 0 || c->top_k < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->n_routed) return MOE_ERR_INVALID_ARG;
+  if (c->gate != MOE_GATE_SOFTMAX && c->gate != MOE_GATE_NOISY) return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_DT_F32 && c->act_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  // noisy top-k always renormalises over the kept entries (softmax of KeepTopK)
+  if (c->gate == MOE_GATE_NOISY && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (c->d % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const int cols = c->gate == MOE_GATE_NOISY ? 2 * c->n_routed : c->n_routed;
+  if (cols > 256 || c->top_k > 32 || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
+  if (c->n_routed + c->n_shared > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  const int64_t rows = c->T * (c->top_k + c->n_shared) + 128ll * (c->n_routed + c->n_shared);
+  if (rows >= (1ll << 31) - 1) return MOE_ERR_UNSUPPORTED;
+  if (c->T * static_cast<int64_t>(c->d) >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+size_t act_bytes(const moe_config* c) { return c->act_dtype == MOE_DT_BF16 ? 2 : 4; }
+
+// ---------------------------------------------------------------------------
+// workspace layouts (every region 256-byte aligned)
+// ---------------------------------------------------------------------------
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return o;
+  }
+};
+
+int64_t n_assign(const moe_config* c) { return c->T * c->top_k; }
+int64_t n_count_blocks(const moe_config* c) { return (n_assign(c) + kCountBlock - 1) / kCountBlock; }
+int32_t n_groups(const moe_config* c) { return c->n_routed + c->n_shared; }
+int64_t padded_rows(const moe_config* c) {
+  // sum over groups of 128 * ceil(rows / 128), bounded above
+  return static_cast<int64_t>(c->n_shared) * ((c->T + 127) / 128) * 128 + n_assign(c) +
+         128ll * c->n_routed;
+}
+
+struct PermuteWs {
+  size_t blk, rank, total;
+};
+PermuteWs permute_layout(const moe_config* c) {
+  Carver k;
+  PermuteWs w;
+  w.blk = k.take(sizeof(int32_t) * n_count_blocks(c) * c->n_routed);
+  w.rank = k.take(sizeof(int32_t) * n_assign(c));
+  w.total = k.off;
+  return w;
+}
+
+struct FfnWs {
+  size_t mt_start, gsize, a_row, o_row, H, total;
+};
+FfnWs ffn_layout(const moe_config* c) {
+  Carver k;
+  FfnWs w;
+  const int G = n_groups(c);
+  w.mt_start = k.take(sizeof(int32_t) * (G + 1));
+  w.gsize = k.take(sizeof(int32_t) * G);
+  w.a_row = k.take(sizeof(int32_t) * G);
+  w.o_row = k.take(sizeof(int32_t) * G);
+  w.H = k.take(act_bytes(c) * padded_rows(c) * c->d_ff);
+  w.total = k.off;
+  return w;
+}
+
+struct FwdWs {
+  size_t ids, w, counts, offsets, dest, perm_src, blk, rank, mt_start, gsize, a_row, o_row, x_perm,
+      H, y_acc, total;
+};
+FwdWs forward_layout(const moe_config* c) {
+  Carver k;
+  FwdWs w;
+  const int64_t n = n_assign(c);
+  const int G = n_groups(c);
+  w.ids = k.take(sizeof(int32_t) * n);
+  w.w = k.take(sizeof(float) * n);
+  w.counts = k.take(sizeof(int32_t) * c->n_routed);
+  w.offsets = k.take(sizeof(int32_t) * (c->n_routed + 1));
+  w.dest = k.take(sizeof(int32_t) * n);
+  w.perm_src = k.take(sizeof(int32_t) * n);
+  w.blk = k.take(sizeof(int32_t) * n_count_blocks(c) * c->n_routed);
+  w.rank = k.take(sizeof(int32_t) * n);
+  w.mt_start = k.take(sizeof(int32_t) * (G + 1));
+  w.gsize = k.take(sizeof(int32_t) * G);
+  w.a_row = k.take(sizeof(int32_t) * G);
+  w.o_row = k.take(sizeof(int32_t) * G);
+  w.x_perm = k.take(act_bytes(c) * n * c->d);
+  w.H = k.take(act_bytes(c) * padded_rows(c) * c->d_ff);
+  w.y_acc = c->act_dtype == MOE_DT_BF16 ? k.take(sizeof(float) * c->T * c->d) : 0;
+  w.total = k.off;
+  return w;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// per-device state: SM count, kernel attributes, the tensor-map encoder
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+};
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+moe_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MOE_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    bool ok = true;
+    ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tc_smem_bytes(kEpiSwiGLU))) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiStoreRows>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tc_smem_bytes(kEpiStoreRows))) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiScatterAdd>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tc_smem_bytes(kEpiScatterAdd))) == cudaSuccess;
+#define MOE_ROUTER_ATTR(TX, EP)                                                                  \
+  ok &= cudaFuncSetAttribute(router_kernel<TX, EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(router_smem_bytes<EP>())) == cudaSuccess;
+    MOE_ROUTER_ATTR(float, 32) MOE_ROUTER_ATTR(float, 64) MOE_ROUTER_ATTR(float, 128)
+    MOE_ROUTER_ATTR(float, 256) MOE_ROUTER_ATTR(__nv_bfloat16, 32)
+    MOE_ROUTER_ATTR(__nv_bfloat16, 64) MOE_ROUTER_ATTR(__nv_bfloat16, 128)
+    MOE_ROUTER_ATTR(__nv_bfloat16, 256)
+#undef MOE_ROUTER_ATTR
+    if (!ok) return MOE_ERR_CUDA;
+    s.ready = true;
+  }
+  *out = &s;
+  return MOE_OK;
+}
+
+moe_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uint32_t esize,
+                    uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                    CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[2] = {cols, rows > 0 ? rows : 1};
+  const cuuint64_t strides[1] = {cols * esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                   \
+  do {                                  \
+    const moe_status _s = (expr);       \
+    if (_s != MOE_OK) return _s;        \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// stages
+// ---------------------------------------------------------------------------
+moe_status launch_route(const moe_config* c, const void* x, const float* W_g, const float* W_noise,
+                        const float* eps, const float* bias, int32_t* ids, float* w, float* logits,
+                        float* zero_rows, cudaStream_t st) {
+  RouterArgs a;
+  a.x = x;
+  a.W_g = W_g;
+  a.W_noise = W_noise;
+  a.eps = eps;
+  a.bias = bias;
+  a.topk_ids = ids;
+  a.topk_w = w;
+  a.logits_out = logits;
+  a.zero_rows = zero_rows;
+  a.T = c->T;
+  a.d = c->d;
+  a.E = c->n_routed;
+  a.k = c->top_k;
+  a.renorm = c->renormalize;
+  a.noisy = c->gate == MOE_GATE_NOISY;
+  a.zero_width = c->d;
+  const int cols = a.noisy ? 2 * a.E : a.E;
+  const unsigned grid = static_cast<unsigned>((c->T + kRouterBT - 1) / kRouterBT);
+  if (grid == 0) return MOE_OK;
+  const bool bf = c->act_dtype == MOE_DT_BF16;
+#define MOE_ROUTE(EP)                                                                            \
+  if (bf)                                                                                        \
+    router_kernel<__nv_bfloat16, EP><<<grid, kRouterThreads, router_smem_bytes<EP>(), st>>>(a);  \
+  else                                                                                           \
+    router_kernel<float, EP><<<grid, kRouterThreads, router_smem_bytes<EP>(), st>>>(a);
+  if (cols <= 32) { MOE_ROUTE(32) }
+  else if (cols <= 64) { MOE_ROUTE(64) }
+  else if (cols <= 128) { MOE_ROUTE(128) }
+  else { MOE_ROUTE(256) }
+#undef MOE_ROUTE
+  return last_launch();
+}
+
+moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void* x,
+                          const int32_t* ids, int32_t* blk, int32_t* rank, int32_t* counts,
+                          int32_t* offsets, int32_t* dest, int32_t* perm_src, void* x_perm,
+                          const PlanOut* plan, cudaStream_t st) {
+  const int64_t n = n_assign(c);
+  const int64_t nblk = n_count_blocks(c);
+  const int E = c->n_routed;
+  if (nblk > 0) {
+    count_kernel<<<static_cast<unsigned>(nblk), kCountThreads, 8 * E * sizeof(int32_t), st>>>(
+        ids, n, E, blk, rank);
+    MOE_TRY(last_launch());
+  }
+  PlanOut none{};
+  scan_kernel<<<1, kScanThreads, 0, st>>>(blk, static_cast<int32_t>(nblk), E, counts, offsets,
+                                          c->n_shared, c->T, plan ? *plan : none, plan ? 1 : 0);
+  MOE_TRY(last_launch());
+  if (n > 0) {
+    const int64_t want = (n + 7) / 8;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, 16ll * ds->sm_count));
+    if (c->act_dtype == MOE_DT_BF16)
+      scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          ids, n, c->top_k, E, blk, rank, static_cast<const __nv_bfloat16*>(x), c->d, dest,
+          perm_src, static_cast<__nv_bfloat16*>(x_perm));
+    else
+      scatter_kernel<float><<<grid, 256, 0, st>>>(ids, n, c->top_k, E, blk, rank,
+                                                  static_cast<const float*>(x), c->d, dest,
+                                                  perm_src, static_cast<float*>(x_perm));
+    MOE_TRY(last_launch());
+  }
+  return MOE_OK;
+}
+
+// Gate-up (SwiGLU fused) into H, then the down projection with epilogue `mode`.
+moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void* x,
+                          const void* x_perm, const GroupPlan& plan, const void* W1, const void* W3,
+                          const void* W2, void* H, int mode, float* out, const int32_t* perm_src,
+                          const float* topk_w, cudaStream_t st,
+                          const std::function<moe_status(int)>* mark = nullptr) {
+  const int G = n_groups(c);
+  const int64_t P = padded_rows(c);
+  const int I = c->d_ff, d = c->d;
+  if (c->act_dtype == MOE_DT_BF16) {
+    TcMaps gu{}, dn{};
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    MOE_TRY(make_map(&gu.a0, x, bf, 2, d, c->T, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(make_map(&gu.a1, x_perm, bf, 2, d, n_assign(c), kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(make_map(&gu.b0, W1, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(make_map(&gu.b1, W3, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(make_map(&gu.out, H, bf, 2, I, P, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
+    MOE_TRY(make_map(&dn.a0, H, bf, 2, I, P, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(make_map(&dn.b0, W2, bf, 2, I, static_cast<uint64_t>(G) * d, kTcBK, kTcBN,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+    dn.a1 = dn.a0;
+    dn.b1 = dn.b0;
+    dn.out = dn.a0;
+
+    TcArgs a{};
+    a.plan = plan;
+    a.G = G;
+    a.n_shared = c->n_shared;
+    a.top_k = c->top_k;
+    a.perm_src = perm_src;
+    a.topk_w = topk_w;
+    const unsigned grid = static_cast<unsigned>(ds->sm_count);
+
+    a.K = d;
+    a.n_tiles = (I + kTcBN / 2 - 1) / (kTcBN / 2);
+    a.b_rows = I;
+    a.n_out = I;
+    grouped_gemm_tc<kEpiSwiGLU><<<grid, kTcThreads, tc_smem_bytes(kEpiSwiGLU), st>>>(gu, a);
+    MOE_TRY(last_launch());
+    if (mark) MOE_TRY((*mark)(3));
+
+    a.K = I;
+    a.n_tiles = (d + kTcBN - 1) / kTcBN;
+    a.b_rows = d;
+    a.n_out = d;
+    a.out = out;
+    if (mode == kEpiScatterAdd)
+      grouped_gemm_tc<kEpiScatterAdd><<<grid, kTcThreads, tc_smem_bytes(kEpiScatterAdd), st>>>(dn, a);
+    else
+      grouped_gemm_tc<kEpiStoreRows><<<grid, kTcThreads, tc_smem_bytes(kEpiStoreRows), st>>>(dn, a);
+    MOE_TRY(last_launch());
+    return mark ? (*mark)(4) : MOE_OK;
+  }
+  SimtArgs a{};
+  a.plan = plan;
+  a.G = G;
+  a.n_shared = c->n_shared;
+  a.top_k = c->top_k;
+  a.perm_src = perm_src;
+  a.topk_w = topk_w;
+  const unsigned grid = static_cast<unsigned>(4 * ds->sm_count);
+  a.K = d;
+  a.n_out = I;
+  a.b_rows = I;
+  a.a0 = static_cast<const float*>(x);
+  a.a1 = static_cast<const float*>(x_perm);
+  a.b0 = static_cast<const float*>(W1);
+  a.b1 = static_cast<const float*>(W3);
+  a.h_out = static_cast<float*>(H);
+  grouped_gemm_simt<kEpiSwiGLU><<<grid, kSimtThreads, 0, st>>>(a);
+  MOE_TRY(last_launch());
+  if (mark) MOE_TRY((*mark)(3));
+  a.K = I;
+  a.n_out = d;
+  a.b_rows = d;
+  a.a0 = static_cast<const float*>(H);
+  a.a1 = nullptr;
+  a.b0 = static_cast<const float*>(W2);
+  a.b1 = nullptr;
+  a.out = out;
+  if (mode == kEpiScatterAdd)
+    grouped_gemm_simt<kEpiScatterAdd><<<grid, kSimtThreads, 0, st>>>(a);
+  else
+    grouped_gemm_simt<kEpiStoreRows><<<grid, kSimtThreads, 0, st>>>(a);
+  MOE_TRY(last_launch());
+  return mark ? (*mark)(4) : MOE_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// extern "C" entry points
+// ===========================================================================
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: configuration outside the kernels' limits";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a kernel wait exceeded its limit";
+    case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX: expert id out of range on the device";
+    default: return "unknown moe_status";
+  }
+}
+
+int moe_version(void) { return kVersion; }
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                     const float* eps, const float* bias, int32_t* topk_ids, float* topk_w,
+                     float* logits, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const bool noisy = cfg->gate == MOE_GATE_NOISY;
+  if (cfg->T > 0 && (x == nullptr || W_g == nullptr || topk_ids == nullptr || topk_w == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (noisy && cfg->T > 0 && (W_noise == nullptr || eps == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x)) return MOE_ERR_INVALID_ARG;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  return launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, topk_ids,
+                      topk_w, logits, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_permute_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return permute_layout(cfg).total;
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                       void* workspace, size_t ws_bytes, int32_t* counts, int32_t* offsets,
+                       int32_t* dest, int32_t* perm_src, void* x_perm, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (counts == nullptr || offsets == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (x == nullptr || topk_ids == nullptr || dest == nullptr || perm_src == nullptr ||
+                     x_perm == nullptr || workspace == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const PermuteWs L = permute_layout(cfg);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  return launch_permute(cfg, ds, x, topk_ids, at<int32_t>(workspace, L.blk),
+                        at<int32_t>(workspace, L.rank), counts, offsets, dest, perm_src, x_perm,
+                        nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_expert_ffn_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return ffn_layout(cfg).total;
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x, const void* x_perm,
+                          const int32_t* offsets, const void* W1, const void* W3, const void* W2,
+                          void* workspace, size_t ws_bytes, float* out_rows, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (x == nullptr || x_perm == nullptr || offsets == nullptr || W1 == nullptr || W3 == nullptr ||
+      W2 == nullptr || workspace == nullptr || out_rows == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) ||
+      !aligned16(workspace) || !aligned16(out_rows))
+    return MOE_ERR_INVALID_ARG;
+  const FfnWs L = ffn_layout(cfg);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
+             at<int32_t>(workspace, L.a_row), at<int32_t>(workspace, L.o_row)};
+  plan_kernel<<<1, 512, 0, st>>>(offsets, cfg->n_routed, cfg->n_shared, cfg->T, po);
+  MOE_TRY(last_launch());
+  GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
+  return launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H), kEpiStoreRows,
+                        out_rows, nullptr, nullptr, st);
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* out_rows, const int32_t* dest,
+                       const float* topk_w, void* y, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (out_rows == nullptr || dest == nullptr || topk_w == nullptr || y == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(out_rows) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(cfg->T);
+  if (cfg->act_dtype == MOE_DT_BF16)
+    combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(out_rows, dest, topk_w, cfg->T, cfg->d,
+                                                        cfg->top_k, cfg->n_shared,
+                                                        static_cast<__nv_bfloat16*>(y));
+  else
+    combine_kernel<float><<<grid, 256, 0, st>>>(out_rows, dest, topk_w, cfg->T, cfg->d, cfg->top_k,
+                                                cfg->n_shared, static_cast<float*>(y));
+  return last_launch();
+}
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return forward_layout(cfg).total;
+}
+
+moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const float* W_g,
+                                const float* W_noise, const float* eps, const float* bias,
+                                const void* W1, const void* W3, const void* W2, void* workspace,
+                                size_t ws_bytes, void* y, int32_t* topk_ids_out, float* topk_w_out,
+                                int32_t* counts_out, void* stream, void* const* stage_events) {
+  MOE_TRY(check_config(cfg));
+  const bool noisy = cfg->gate == MOE_GATE_NOISY;
+  if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (x == nullptr || W_g == nullptr || W1 == nullptr || W3 == nullptr || W2 == nullptr ||
+      workspace == nullptr || y == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (noisy && (W_noise == nullptr || eps == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(workspace) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const FwdWs L = forward_layout(cfg);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf = cfg->act_dtype == MOE_DT_BF16;
+
+  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float>(workspace, L.w);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(workspace, L.counts);
+  float* acc = bf ? at<float>(workspace, L.y_acc) : static_cast<float*>(y);
+
+  const std::function<moe_status(int)> mark = [&](int i) -> moe_status {
+    if (stage_events == nullptr) return MOE_OK;
+    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st) == cudaSuccess ? MOE_OK
+                                                                                          : MOE_ERR_CUDA;
+  };
+  MOE_TRY(mark(0));
+  // 1. gate (also clears the fp32 accumulator rows of its tokens)
+  MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w,
+                       nullptr, acc, st));
+  MOE_TRY(mark(1));
+  // 2. dispatch + group plan
+  PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
+             at<int32_t>(workspace, L.a_row), at<int32_t>(workspace, L.o_row)};
+  int32_t* perm_src = at<int32_t>(workspace, L.perm_src);
+  void* x_perm = at<void>(workspace, L.x_perm);
+  MOE_TRY(launch_permute(cfg, ds, x, ids, at<int32_t>(workspace, L.blk),
+                         at<int32_t>(workspace, L.rank), counts, at<int32_t>(workspace, L.offsets),
+                         at<int32_t>(workspace, L.dest), perm_src, x_perm, &po, st));
+  MOE_TRY(mark(2));
+  // 3. experts: gate-up + SwiGLU, then down with the gate-weighted scatter-add
+  GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
+  MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H),
+                         kEpiScatterAdd, acc, perm_src, w, st, stage_events ? &mark : nullptr));
+  // 4. fp32 accumulator -> bf16 output
+  if (bf) {
+    const int64_t n8 = cfg->T * cfg->d / 8;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n8 + 255) / 256, 8ll * ds->sm_count));
+    cast_bf16_kernel<<<grid, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(y), n8);
+    MOE_TRY(last_launch());
+  }
+  return mark(5);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                       const float* eps, const float* bias, const void* W1, const void* W3,
+                       const void* W2, void* workspace, size_t ws_bytes, void* y,
+                       int32_t* topk_ids_out, float* topk_w_out, int32_t* counts_out,
+                       void* stream) {
+  return moe_forward_profiled(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, workspace, ws_bytes, y,
+                              topk_ids_out, topk_w_out, counts_out, stream, nullptr);
+}
+
+moe_status moe_device_status(void* stream, int32_t* raw) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fault_flag, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_fault_flag, &zero, sizeof(zero)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (raw != nullptr) *raw = static_cast<int32_t>(v);
+  if (v & kFaultTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (v & kFaultIndex) return MOE_ERR_DEVICE_INDEX;
+  return MOE_OK;
+}
+
+moe_status moe_debug_wait_timeout(uint32_t limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return MOE_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1000ull * limit_us);
+  return last_launch();
+}
+
+}  // extern "C"

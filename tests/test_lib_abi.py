@@ -1,0 +1,115 @@
+"""The C-ABI library builds, loads and exports every declared symbol (no GPU).
+
+Only host-side paths run here: sizes, status strings and argument
+validation, all of which return before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_91_b300 import binding, build, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_b300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and nothing else with the moe_ prefix in the dynamic symbol table
+    out = os.popen(f"nm -D --defined-only {binding._LIB_PATH}").read()
+    exported = sorted(set(re.findall(r"\s(moe_[a-z_0-9]+)$", out, flags=re.M)))
+    assert exported == declared_functions()
+
+
+def test_version_and_status_strings(lib):
+    assert lib.moe_version() >> 16 == 1
+    for s in range(7):
+        assert lib.moe_status_string(s).startswith(b"MOE_")
+    assert b"unknown" in lib.moe_status_string(99)
+
+
+def fwd_nulls(lib, c):
+    return lib.moe_forward(c, None, None, None, None, None, None, None, None, None, 0,
+                           None, None, None, None, None)
+
+
+def cfg_of(**kw):
+    base = dict(T=256, d=128, n_routed=16, n_shared=1, top_k=4, d_ff=64, renormalize=0, gate=0,
+                act_dtype=0)
+    base.update(kw)
+    return binding.MoeConfig(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(top_k=17), dict(top_k=0), dict(d=0), dict(T=-1), dict(n_routed=0), dict(gate=2),
+    dict(act_dtype=5), dict(renormalize=2), dict(gate=1, renormalize=0),
+])
+def test_invalid_configs_rejected(lib, bad):
+    c = cfg_of(**bad)
+    assert lib.moe_workspace_size(ctypes.byref(c)) == 0
+    assert fwd_nulls(lib, ctypes.byref(c)) == 1   # MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [dict(d=12), dict(d_ff=60), dict(n_routed=257),
+                                 dict(gate=1, renormalize=1, n_routed=129), dict(top_k=33, n_routed=64)])
+def test_unsupported_configs(lib, bad):
+    c = cfg_of(**bad)
+    st = lib.moe_route(ctypes.byref(c), *([None] * 8), None)
+    assert st == 2   # MOE_ERR_UNSUPPORTED
+
+
+def test_null_pointers_and_workspace_checked_before_launch(lib):
+    c = cfg_of()
+    assert fwd_nulls(lib, None) == 1
+    assert lib.moe_route(ctypes.byref(c), *([None] * 8), None) == 1
+    # a too-small workspace is reported before anything touches the device
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+    st = lib.moe_forward(ctypes.byref(c), fake, fake, None, None, None, fake, fake, fake, fake, 16,
+                         fake, None, None, None, None)
+    assert st == 3   # MOE_ERR_WORKSPACE
+    misaligned = ctypes.c_void_p((1 << 20) + 4)
+    st = lib.moe_forward(ctypes.byref(c), misaligned, fake, None, None, None, fake, fake, fake, fake,
+                         1 << 40, fake, None, None, None, None)
+    assert st == 1
+
+
+@pytest.mark.parametrize("w", workloads.ALL, ids=lambda w: w.name)
+def test_workspace_sizes_cover_the_buffers(lib, w):
+    c = binding.config(w)
+    ws = lib.moe_workspace_size(ctypes.byref(c))
+    act = 4 if w.fp32 else 2
+    # at least x_perm + H (+ fp32 accumulator)
+    need = act * w.T * w.top_k * w.d + act * (w.n_shared * w.T + w.T * w.top_k) * w.d_ff
+    if not w.fp32:
+        need += 4 * w.T * w.d
+    assert ws >= need
+    assert lib.moe_permute_workspace_size(ctypes.byref(c)) >= 4 * w.T * w.top_k
+    assert lib.moe_expert_ffn_workspace_size(ctypes.byref(c)) >= act * (w.n_shared * w.T + w.T * w.top_k) * w.d_ff
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    c = cfg_of(T=0)
+    assert fwd_nulls(lib, ctypes.byref(c)) == 0
+    assert lib.moe_expert_ffn(ctypes.byref(c), None, None, None, None, None, None, None, 0, None,
+                              None) == 0
+    assert lib.moe_combine(ctypes.byref(c), None, None, None, None, None) == 0
