@@ -164,6 +164,32 @@ def cpu_oracle_rate(w, inp, budget_s: float) -> dict:
                       f"(numpy/BLAS), {dt:.1f} s"}
 
 
+def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
+    """Per-step time of the public API with pinned-host x (and eps) copied in and
+    y copied out inside the timed region."""
+    x_host = inp["x"].pin_memory()
+    eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
+    y_host = torch.empty(tuple(layer.y.shape), dtype=layer.y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    eps_dev = torch.empty_like(eps) if eps is not None else None
+    for _ in range(args.warmup):
+        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
+    barrier()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
+    e_end.record(stream)
+    barrier()
+    ms = e_start.elapsed_time(e_end) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = tt.item()
+    return ms
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -194,10 +220,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=workloads.HEADLINE.name, choices=sorted(workloads.BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=None, help="override T (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.BY_NAME[args.workload]
+    if args.tokens is not None:
+        w = w.with_tokens(args.tokens)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -252,32 +282,18 @@ def main():
                 for j, n in enumerate(stage_names)}
 
     # ---- end to end through the public API: pinned host x in, host y out
-    x_host = inp["x"].pin_memory()
-    eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
-    y_host = torch.empty(w.T, w.d, dtype=layer.y.dtype, pin_memory=True)
-    x_dev = torch.empty_like(x)
-    eps_dev = torch.empty_like(eps) if eps is not None else None
-    for _ in range(args.warmup):
-        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
-    barrier()
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_start.record(stream)
-    for _ in range(args.steps):
-        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
-    e_end.record(stream)
-    barrier()
-    ms_e2e = e_start.elapsed_time(e_end) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = tt.item()
+    ms_e2e = None
+    if not args.no_e2e:
+        ms_e2e = e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev)
 
     # ---- counts of touched experts for the algorithmic bytes
     _, _, _, counts = binding.forward(layer.cfg, x, layer.W_g, layer.W_noise, eps, layer.bias,
                                       layer.W1, layer.W3, layer.W2, workspace=layer.workspace,
                                       routing=True)
     touched = int((counts > 0).sum().item()) + w.n_shared
+    x_host_bytes = inp["x"].numel() * inp["x"].element_size()
+    eps_bytes = inp["eps"].numel() * 4 if inp["eps"] is not None else 0
+    y_bytes = w.T * w.d * layer.y.element_size()
 
     if rank != 0:
         if world > 1:
@@ -320,10 +336,9 @@ def main():
         "kernels_tflops": {"gate_up": gu_tflops,
                            "down": kf["down"] / (stage_ms["down"] / 1e3) / 1e12,
                            "router": kf["router"] / (stage_ms["router"] / 1e3) / 1e12},
-        "e2e": {"value": world * w.T / (ms_e2e / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": x_host.numel() * x_host.element_size()
-                + (eps_host.numel() * 4 if eps_host is not None else 0),
-                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "e2e": None if ms_e2e is None else {
+            "value": world * w.T / (ms_e2e / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": x_host_bytes + eps_bytes, "d2h_bytes_per_step": y_bytes},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }

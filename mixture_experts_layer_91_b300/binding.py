@@ -225,6 +225,9 @@ def forward_profiled(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, *, workspace, 
     dt = act_dtype(cfg)
     if len(events) != PROFILE_EVENTS:
         raise ValueError(f"need {PROFILE_EVENTS} events")
+    for e in events:          # torch creates the CUDA event on first record
+        if e.cuda_event == 0:
+            e.record()
     arr = (ctypes.c_void_p * PROFILE_EVENTS)(*[e.cuda_event for e in events])
     st = lib.moe_forward_profiled(ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(W_g, torch.float32, "W_g"),
                                   _ptr(W_noise, torch.float32, "W_noise", True),

@@ -520,8 +520,10 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
 
   const std::function<moe_status(int)> mark = [&](int i) -> moe_status {
     if (stage_events == nullptr) return MOE_OK;
-    return cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st) == cudaSuccess ? MOE_OK
-                                                                                          : MOE_ERR_CUDA;
+    if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st) == cudaSuccess) return MOE_OK;
+    cudaGetLastError();   // do not leave the failed record as the runtime's last error
+    return MOE_ERR_CUDA;
   };
   MOE_TRY(mark(0));
   // 1. gate (also clears the fp32 accumulator rows of its tokens)
