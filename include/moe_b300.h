@@ -51,7 +51,8 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,      /* workspace smaller than the *_workspace_size()   */
   MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed               */
   MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired (pipeline fault)*/
-  MOE_ERR_DEVICE_INDEX = 6    /* a kernel met an out-of-range expert id          */
+  MOE_ERR_DEVICE_INDEX = 6,   /* a kernel met an out-of-range expert id          */
+  MOE_ERR_STATIC_LIMIT = 7    /* too large for moe_permute_static's fixed scratch */
 } moe_status;
 
 typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
@@ -126,6 +127,38 @@ size_t moe_permute_workspace_size(const moe_config* cfg);
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_ids,
                        void* workspace, size_t ws_bytes, int32_t* counts, int32_t* offsets,
                        int32_t* dest, int32_t* perm_src, void* x_perm, void* stream);
+
+/* Largest T*k that moe_permute_static accepts (its fixed scratch holds this many). */
+#define MOE_PERMUTE_STATIC_MAX_ASSIGN (1 << 19)
+
+/*
+ * moe_permute_static -- moe_permute without a caller workspace. The paper has
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory for scratch, such as code running under a host framework that
+ * owns the whole device-memory budget and forbids allocation after start-up,
+ * or a serving loop that must never enter an allocator (cudaMalloc/cudaFree
+ * can synchronise the device).
+ *
+ * The scratch (per-block histograms and ranks) is a file-scope device array
+ * of 2.5 MiB in the library, sized for T*k <= MOE_PERMUTE_STATIC_MAX_ASSIGN
+ * (524,288 assignments) and N_r <= 256. Every GPU that loads the library holds
+ * that array until the process exits. Larger problems are rejected with
+ * MOE_ERR_STATIC_LIMIT before anything is enqueued. The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that first
+ * call before any stream capture on that device.
+ *
+ * Sharing: all calls on a device use the same array and it keeps the last
+ * call's contents (the kernels overwrite every entry they read, so nothing has
+ * to start at zero). Calls that overlap on the GPU (different streams, or
+ * different host threads without ordering) race on the array; order them on
+ * one stream. Arguments, outputs and errors are those of moe_permute.
+ */
+moe_status moe_permute_static(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                              int32_t* counts, int32_t* offsets, int32_t* dest,
+                              int32_t* perm_src, void* x_perm, void* stream);
 
 /* Bytes of scratch moe_expert_ffn needs (group plan and the SwiGLU activations). */
 size_t moe_expert_ffn_workspace_size(const moe_config* cfg);

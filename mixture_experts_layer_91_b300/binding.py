@@ -25,11 +25,13 @@ _lock = threading.Lock()
 MOE_DT_F32, MOE_DT_BF16 = 0, 1
 MOE_GATE_SOFTMAX, MOE_GATE_NOISY = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
-          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_DEVICE_INDEX"}
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_DEVICE_INDEX",
+          7: "MOE_ERR_STATIC_LIMIT"}
+PERMUTE_STATIC_MAX_ASSIGN = 1 << 19   # MOE_PERMUTE_STATIC_MAX_ASSIGN
 
 # every symbol include/moe_b300.h declares
 EXPORTS = ["moe_status_string", "moe_version", "moe_route", "moe_permute_workspace_size",
-           "moe_permute", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
+           "moe_permute", "moe_permute_static", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_workspace_size", "moe_forward", "moe_forward_profiled", "moe_device_status",
            "moe_debug_wait_timeout"]
 PROFILE_EVENTS = 6   # MOE_PROFILE_EVENTS
@@ -72,6 +74,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
             "moe_route": (I32, [C, P, P, P, P, P, P, P, P, P]),
             "moe_permute_workspace_size": (SZ, [C]),
             "moe_permute": (I32, [C, P, P, P, SZ, P, P, P, P, P, P]),
+            "moe_permute_static": (I32, [C, P, P, P, P, P, P, P, P]),
             "moe_expert_ffn_workspace_size": (SZ, [C]),
             "moe_expert_ffn": (I32, [C, P, P, P, P, P, P, P, SZ, P, P]),
             "moe_combine": (I32, [C, P, P, P, P, P]),
@@ -165,6 +168,25 @@ def permute(cfg, x, topk_ids, *, stream=None) -> dict:
                          out["counts"].data_ptr(), out["offsets"].data_ptr(), out["dest"].data_ptr(),
                          out["perm_src"].data_ptr(), out["x_perm"].data_ptr(), _stream(stream))
     _check(st, "moe_permute")
+    return out
+
+
+def permute_static(cfg, x, topk_ids, *, stream=None) -> dict:
+    """moe_permute_static: moe_permute with the library's fixed device scratch
+    instead of a workspace (no allocation inside the call)."""
+    lib = load()
+    T, k, E, d = cfg.T, cfg.top_k, cfg.n_routed, cfg.d
+    dev = x.device
+    out = {"counts": torch.empty(E, dtype=torch.int32, device=dev),
+           "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+           "dest": torch.empty(T, k, dtype=torch.int32, device=dev),
+           "perm_src": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "x_perm": torch.empty(T * k, d, dtype=act_dtype(cfg), device=dev)}
+    st = lib.moe_permute_static(ctypes.byref(cfg), _ptr(x, act_dtype(cfg), "x"),
+                                _ptr(topk_ids, torch.int32, "topk_ids"), out["counts"].data_ptr(),
+                                out["offsets"].data_ptr(), out["dest"].data_ptr(),
+                                out["perm_src"].data_ptr(), out["x_perm"].data_ptr(), _stream(stream))
+    _check(st, "moe_permute_static")
     return out
 
 

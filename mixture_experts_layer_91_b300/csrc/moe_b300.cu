@@ -375,6 +375,35 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
   return mark ? (*mark)(4) : MOE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// fixed scratch of moe_permute_static (no caller workspace, no allocation)
+// ---------------------------------------------------------------------------
+constexpr int64_t kStaticMaxAssign = MOE_PERMUTE_STATIC_MAX_ASSIGN;
+constexpr int kStaticMaxExperts = 256;
+constexpr int64_t kStaticMaxBlocks = kStaticMaxAssign / kCountBlock;
+constexpr int64_t kStaticScratchInts = kStaticMaxBlocks * kStaticMaxExperts + kStaticMaxAssign;
+
+// Per-block histograms ([blocks][N_r], blocks <= kStaticMaxBlocks) followed by
+// the per-assignment ranks. Shared by every call on the device.
+static __device__ __align__(256) int32_t g_permute_scratch[kStaticScratchInts];
+
+int32_t* g_static_scratch[kMaxDevices] = {};
+
+// Device address of g_permute_scratch on the current device, looked up once
+// per device (host code must not use the symbol itself as a device pointer).
+moe_status static_scratch(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_static_scratch[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_static_scratch[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_static_scratch[dev];
+  return MOE_OK;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -391,6 +420,8 @@ const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
     case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a kernel wait exceeded its limit";
     case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX: expert id out of range on the device";
+    case MOE_ERR_STATIC_LIMIT:
+      return "MOE_ERR_STATIC_LIMIT: T*k or N_r exceeds the fixed scratch of moe_permute_static";
     default: return "unknown moe_status";
   }
 }
@@ -433,6 +464,26 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   MOE_TRY(device_state(&ds));
   return launch_permute(cfg, ds, x, topk_ids, at<int32_t>(workspace, L.blk),
                         at<int32_t>(workspace, L.rank), counts, offsets, dest, perm_src, x_perm,
+                        nullptr, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute_static(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                              int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* perm_src,
+                              void* x_perm, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (n_assign(cfg) > kStaticMaxAssign || cfg->n_routed > kStaticMaxExperts) return MOE_ERR_STATIC_LIMIT;
+  if (counts == nullptr || offsets == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (x == nullptr || topk_ids == nullptr || dest == nullptr || perm_src == nullptr ||
+                     x_perm == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  int32_t* scratch;
+  MOE_TRY(static_scratch(&scratch));
+  int32_t* blk = scratch;
+  int32_t* rank = scratch + kStaticMaxBlocks * kStaticMaxExperts;
+  return launch_permute(cfg, ds, x, topk_ids, blk, rank, counts, offsets, dest, perm_src, x_perm,
                         nullptr, static_cast<cudaStream_t>(stream));
 }
 

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.moe_version() >> 16 == 1
-    for s in range(7):
+    for s in range(8):
         assert lib.moe_status_string(s).startswith(b"MOE_")
     assert b"unknown" in lib.moe_status_string(99)
 
