@@ -22,8 +22,10 @@
 //               32-lane quarter), then
 //                 gate-up : h = silu(acc[:, 0:128]) * acc[:, 128:256] -> bf16,
 //                           staged in shared memory, TMA-stored to H;
-//                 down    : acc * gate red.add'ed into y_acc[token] (fp32), or
-//                           stored as fp32 rows (stage entry point).
+//                 down    : acc * gate, transposed in registers so each warp
+//                           instruction adds one 128-byte row segment
+//                           (red.global.add.f32) into y_acc[token]; or stored
+//                           as fp32 rows (stage entry point).
 //
 // The gate-up B tile stacks 128 rows of W1 over the same 128 rows of W3, so
 // one N=256 MMA produces the gate and up halves of the same output columns
@@ -250,10 +252,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TileCoord c = decode_tile(t, p.n_tiles, p.plan.mt_start, p.G);
       const uint32_t b = local & 1u;
       const uint32_t aph = (local >> 1) & 1u;
+      const int32_t row_local = c.lmt * kTcBM + q * 32 + lane;
+      // Row bookkeeping of the down epilogues, loaded before the accumulator is
+      // ready so the dependent global loads overlap the tile's MMAs.
+      bool valid = false;
+      int64_t orow = 0;
+      float gate = 1.0f;
+      if (MODE != kEpiSwiGLU) {
+        valid = row_local < __ldg(p.plan.gsize + c.g);
+        if (valid) {
+          if (MODE == kEpiScatterAdd) {
+            if (c.g < p.n_shared) {
+              orow = row_local;   // shared expert: row = token, gate 1
+            } else {
+              const int32_t src = __ldg(p.perm_src + __ldg(p.plan.a_row + c.g) + row_local);
+              orow = src / p.top_k;
+              gate = __ldg(p.topk_w + src);
+            }
+          } else {
+            orow = static_cast<int64_t>(__ldg(p.plan.o_row + c.g)) + row_local;
+          }
+        }
+      }
       if (!mbar_wait(bar_tfull + 8 * b, aph, abort)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kTcBN;
-      const int32_t row_local = c.lmt * kTcBM + q * 32 + lane;
 
       if (MODE == kEpiSwiGLU) {
         const uint32_t buf0 = sStore + ew * 2 * kStoreBoxBytes;
@@ -290,23 +313,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bulk_commit();
           }
         }
-      } else {
-        const bool valid = row_local < __ldg(p.plan.gsize + c.g);
-        int64_t orow = 0;
-        float gate = 1.0f;
-        if (valid) {
-          if (MODE == kEpiScatterAdd) {
-            if (c.g < p.n_shared) {
-              orow = row_local;   // shared expert: row = token, gate 1
-            } else {
-              const int32_t src = __ldg(p.perm_src + __ldg(p.plan.a_row + c.g) + row_local);
-              orow = src / p.top_k;
-              gate = __ldg(p.topk_w + src);
+      } else if (MODE == kEpiScatterAdd) {
+        // Gate-scaled rows added into y_acc[token]. A 32x32 register transpose
+        // (five xor-shuffle stages) gives each lane one column of the warp's 32
+        // rows, so every red.global.add covers a full 128-byte row segment.
+        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+        int32_t tok[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) tok[r] = __shfl_sync(0xffffffffu, static_cast<int32_t>(orow), r);
+#pragma unroll 1
+        for (int cc = 0; cc < kTcBN / 32; ++cc) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tacc + cc * 32, raw);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]) * gate;
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i & m) continue;
+              const float send = upper ? v[i] : v[i | m];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+              if (upper) v[i] = recv; else v[i | m] = recv;
             }
-          } else {
-            orow = static_cast<int64_t>(__ldg(p.plan.o_row + c.g)) + row_local;
+          }
+          // lane now holds column `col` of rows 0..31 of this warp's quarter
+          const int32_t col = c.nt * kTcBN + cc * 32 + lane;
+          if (col < p.n_out) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              if ((vmask >> r) & 1u)
+                asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p.out + static_cast<int64_t>(tok[r]) * p.n_out + col),
+                             "f"(v[r])
+                             : "memory");
           }
         }
+      } else {
         float* dst = p.out + orow * p.n_out;
 #pragma unroll 1
         for (int cc = 0; cc < kTcBN / 32; ++cc) {
@@ -318,17 +363,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int32_t col = col0 + 4 * j;
-              if (col < p.n_out) {
-                const float a = __uint_as_float(v[4 * j]) * gate;
-                const float bq = __uint_as_float(v[4 * j + 1]) * gate;
-                const float cq = __uint_as_float(v[4 * j + 2]) * gate;
-                const float dq = __uint_as_float(v[4 * j + 3]) * gate;
-                if (MODE == kEpiScatterAdd) {
-                  red_add_v4(dst + col, a, bq, cq, dq);
-                } else {
-                  *reinterpret_cast<float4*>(dst + col) = make_float4(a, bq, cq, dq);
-                }
-              }
+              if (col < p.n_out)
+                *reinterpret_cast<float4*>(dst + col) =
+                    make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
             }
           }
         }
