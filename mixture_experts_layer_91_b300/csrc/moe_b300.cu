@@ -218,7 +218,7 @@ moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : M
 // ---------------------------------------------------------------------------
 moe_status launch_route(const moe_config* c, const void* x, const float* W_g, const float* W_noise,
                         const float* eps, const float* bias, int32_t* ids, float* w, float* logits,
-                        float* zero_rows, cudaStream_t st) {
+                        float* zero_rows, int sm_count, cudaStream_t st) {
   RouterArgs a;
   a.x = x;
   a.W_g = W_g;
@@ -236,20 +236,41 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   a.renorm = c->renormalize;
   a.noisy = c->gate == MOE_GATE_NOISY;
   a.zero_width = c->d;
+  a.w_vec4 = (c->n_routed % 4 == 0) && aligned16(W_g) && (W_noise == nullptr || aligned16(W_noise));
   const int cols = a.noisy ? 2 * a.E : a.E;
-  const unsigned grid = static_cast<unsigned>((c->T + kRouterBT - 1) / kRouterBT);
-  if (grid == 0) return MOE_OK;
+  const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
+  if (nblk == 0) return MOE_OK;
+  // Few token blocks (decode-sized T): a cluster of CS CTAs also splits the
+  // k-chunks, until there are about two CTAs per SM or two chunks per CTA.
+  const int nchunk = (c->d + kRouterBK - 1) / kRouterBK;
+  int cs = 1;
+  while (cs < 8 && nblk * cs < 2ll * sm_count && nchunk >= 4 * cs) cs *= 2;
+  cudaLaunchConfig_t lc{};
+  cudaLaunchAttribute attr[1];
+  lc.gridDim = dim3(static_cast<unsigned>(nblk * cs), 1, 1);
+  lc.blockDim = dim3(kRouterThreads, 1, 1);
+  lc.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
   const bool bf = c->act_dtype == MOE_DT_BF16;
-#define MOE_ROUTE(EP)                                                                            \
-  if (bf)                                                                                        \
-    router_kernel<__nv_bfloat16, EP><<<grid, kRouterThreads, router_smem_bytes<EP>(), st>>>(a);  \
-  else                                                                                           \
-    router_kernel<float, EP><<<grid, kRouterThreads, router_smem_bytes<EP>(), st>>>(a);
+  cudaError_t e;
+#define MOE_ROUTE(EP)                                                                \
+  lc.dynamicSmemBytes = router_smem_bytes<EP>();                                     \
+  e = bf ? cudaLaunchKernelEx(&lc, router_kernel<__nv_bfloat16, EP>, a)              \
+         : cudaLaunchKernelEx(&lc, router_kernel<float, EP>, a);
   if (cols <= 32) { MOE_ROUTE(32) }
   else if (cols <= 64) { MOE_ROUTE(64) }
   else if (cols <= 128) { MOE_ROUTE(128) }
   else { MOE_ROUTE(256) }
 #undef MOE_ROUTE
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
   return last_launch();
 }
 
@@ -441,7 +462,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, con
   DeviceState* ds;
   MOE_TRY(device_state(&ds));
   return launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, topk_ids,
-                      topk_w, logits, nullptr, static_cast<cudaStream_t>(stream));
+                      topk_w, logits, nullptr, ds->sm_count, static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_permute_workspace_size(const moe_config* cfg) {
@@ -579,7 +600,7 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   MOE_TRY(mark(0));
   // 1. gate (also clears the fp32 accumulator rows of its tokens)
   MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w,
-                       nullptr, acc, st));
+                       nullptr, acc, ds->sm_count, st));
   MOE_TRY(mark(1));
   // 2. dispatch + group plan
   PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),

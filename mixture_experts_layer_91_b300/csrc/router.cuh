@@ -9,11 +9,18 @@
 // The router runs in fp32 because routing is sensitive to rounding
 // ("Mixture of Experts" notes, section 5, ST-MoE precision discussion).
 //
-// One CTA handles BT = 64 tokens and every router column (N_r, or 2 N_r when
-// the noise projection is concatenated). CUDA-core FMA GEMM through shared
-// memory; the [64 x cols] logits tile then stays in shared memory, where one
-// warp per token computes the softmax and a k-round warp arg-max (ties to the
-// lower expert index).
+// Layout of the work. One CTA owns BT = 32 tokens and every router column
+// (N_r, or 2 N_r with the noise projection concatenated as [W_g | W_noise]).
+// Its 8 warps split the reduction over d: each warp computes the whole
+// 32 x EPAD logits tile over its share of every 64-deep k-chunk, one thread
+// holding an 8 x 8 (or 4 x 16 / 4 x 32) register tile, so each k-step costs
+// two or three conflict-free 16-byte shared loads per 32-128 FMAs. Chunks are
+// double-buffered: W through cp.async, x through registers (widened to fp32 on
+// the way into shared memory). The per-warp partial tiles are summed in shared
+// memory in a fixed order. When T is small a thread-block cluster of CS CTAs
+// also splits the k-chunks, and the leader CTA adds the other CTAs' tiles
+// through distributed shared memory. The leader then computes, one warp per
+// token, the softmax and a k-round warp arg-max (ties to the lower index).
 #pragma once
 
 #include "common.cuh"
@@ -32,19 +39,33 @@ struct RouterArgs {
   float* zero_rows;      // [T, zero_width] fp32 rows to clear, or null (fused y_acc clear)
   int64_t T;
   int32_t d, E, k, renorm, noisy, zero_width;
+  int32_t w_vec4;        // W rows may be copied in 16-byte pieces (E % 4 == 0, aligned)
 };
 
-constexpr int kRouterBT = 64;       // tokens per CTA
-constexpr int kRouterBK = 32;       // k-chunk staged in shared memory
+constexpr int kRouterBT = 32;       // tokens per CTA
+constexpr int kRouterBK = 64;       // k-chunk staged in shared memory
 constexpr int kRouterThreads = 256;
+constexpr int kRouterWarps = kRouterThreads / 32;
+constexpr int kRouterXS = kRouterBT + 4;   // row stride of the staged x^T chunk
 
 template <int EPAD>
-constexpr size_t router_smem_bytes() {
-  // staging: xs [BK][BT+4] + ws [BK][EPAD]; logits tile [BT][EPAD+1]
-  constexpr size_t stage = (kRouterBK * (kRouterBT + 4) + kRouterBK * EPAD) * sizeof(float);
-  constexpr size_t tile = static_cast<size_t>(kRouterBT) * (EPAD + 1) * sizeof(float);
-  return stage > tile ? stage : tile;
-}
+struct RouterShape {
+  static constexpr int TN = EPAD / 8;            // columns per thread (8 column groups per warp)
+  static constexpr int TM = EPAD <= 64 ? 8 : 4;  // tokens per thread (4 token groups per warp)
+  static constexpr int WT = 4 * TM;              // tokens per warp tile
+  static constexpr int WROWS = kRouterBT / WT;   // warp rows covering the CTA's tokens
+  static constexpr int SPLIT = kRouterWarps / WROWS;   // warps sharing one k-chunk
+  static constexpr int LS = EPAD + 1;            // row stride of the logits tiles
+  static constexpr size_t stage_floats = kRouterBK * kRouterXS + kRouterBK * EPAD;
+  static constexpr size_t part_floats = static_cast<size_t>(SPLIT) * kRouterBT * LS;
+  static constexpr size_t smem_bytes =
+      (2 * stage_floats > part_floats ? 2 * stage_floats : part_floats) * sizeof(float);
+  static_assert(WROWS * WT == kRouterBT && SPLIT * WROWS == kRouterWarps, "router tiling");
+  static_assert(kRouterBK % SPLIT == 0 && TN % 4 == 0 && TM % 4 == 0, "router tiling");
+};
+
+template <int EPAD>
+constexpr size_t router_smem_bytes() { return RouterShape<EPAD>::smem_bytes; }
 
 __device__ __forceinline__ float softplus_f(float z) { return z > 20.0f ? z : log1pf(expf(z)); }
 
@@ -54,27 +75,144 @@ __device__ __forceinline__ bool better(float ka, int ia, float kb, int ib) {
   return (ka > kb) || (ka == kb && ia < ib);
 }
 
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// x chunk [BT tokens][BK] -> registers: thread -> token tid % 32, k sub-range
+// (tid / 32) * 8 .. + 8 (one 16-byte load for bf16, two for fp32). Kept raw
+// until the store so the prefetch costs as few registers as possible.
+template <typename TX>
+struct XFrag {
+  uint4 u[sizeof(TX) / 2];
+};
+
+template <typename TX>
+__device__ __forceinline__ void load_x_frag(XFrag<TX>& f, const TX* x, int64_t T, int32_t d,
+                                            int64_t t0, int k0, int tid) {
+  const int64_t t = t0 + (tid & 31);
+  const int kg = k0 + (tid >> 5) * 8;
+  const bool ok = t < T && kg < d;   // d % 8 == 0: a vector is entirely in or out
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(TX) / 2); ++i)
+    f.u[i] = ok ? __ldg(reinterpret_cast<const uint4*>(x + t * d + kg) + i) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <typename TX>
+__device__ __forceinline__ void store_x_frag(const XFrag<TX>& f, float* xs, int tid) {
+  const int tok = tid & 31;
+  const int kk = (tid >> 5) * 8;
+  float v[8];
+  if constexpr (sizeof(TX) == 2) {
+    const uint32_t w[4] = {f.u[0].x, f.u[0].y, f.u[0].z, f.u[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // bf16 -> fp32 is exact: the bf16 bits are the high half
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+    const uint32_t w[8] = {f.u[0].x, f.u[0].y, f.u[0].z, f.u[0].w, f.u[1].x, f.u[1].y, f.u[1].z, f.u[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(w[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) xs[(kk + i) * kRouterXS + tok] = v[i];
+}
+
+// W chunk rows k0..k0+BK, columns [0, EPAD) of [W_g | W_noise] -> ws, async.
+template <int EPAD>
+__device__ __forceinline__ void load_w_chunk(float* ws, const RouterArgs& p, int ncols, int k0, int tid) {
+  const uint32_t base = smem_addr(ws);
+  if (p.w_vec4) {
+    constexpr int V = EPAD / 4;
+    for (int idx = tid; idx < kRouterBK * V; idx += kRouterThreads) {
+      const int r = idx / V, c = (idx % V) * 4;
+      const int kg = k0 + r;
+      const float* src = p.W_g;
+      uint32_t n = 0;
+      if (kg < p.d && c < ncols) {
+        src = (c < p.E) ? p.W_g + static_cast<int64_t>(kg) * p.E + c
+                        : p.W_noise + static_cast<int64_t>(kg) * p.E + (c - p.E);
+        n = 16;
+      }
+      cp_async16(base + (r * EPAD + c) * 4, src, n);
+    }
+  } else {
+    for (int idx = tid; idx < kRouterBK * EPAD; idx += kRouterThreads) {
+      const int r = idx / EPAD, c = idx % EPAD;
+      const int kg = k0 + r;
+      const float* src = p.W_g;
+      uint32_t n = 0;
+      if (kg < p.d && c < ncols) {
+        src = (c < p.E) ? p.W_g + static_cast<int64_t>(kg) * p.E + c
+                        : p.W_noise + static_cast<int64_t>(kg) * p.E + (c - p.E);
+        n = 4;
+      }
+      cp_async4(base + idx * 4, src, n);
+    }
+  }
+}
+
 template <typename TX, int EPAD>
-__global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs p) {
-  constexpr int TN = EPAD / 16;  // columns per thread
-  constexpr int TM = 4;          // tokens per thread
-  constexpr int XS = kRouterBT + 4;
+__global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_kernel(const RouterArgs p) {
+  using S = RouterShape<EPAD>;
+  constexpr int TM = S::TM, TN = S::TN;
   extern __shared__ __align__(16) float rsm[];
-  float* xs = rsm;                         // [BK][XS]
-  float* ws = rsm + kRouterBK * XS;        // [BK][EPAD]
 
   const int tid = threadIdx.x;
-  const int tx = tid & 15;   // column group
-  const int ty = tid >> 4;   // token group
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouterBT;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int tg = lane >> 3, cg = lane & 7;          // token group, column group of this lane
+  const int wr = warp / S::SPLIT;                   // warp row
+  const int ks = warp % S::SPLIT;                   // k-step phase of this warp inside a chunk
+  const int tok0 = wr * S::WT + tg * TM;            // first token (CTA-local) of the thread tile
+
+  const uint32_t crank = cluster_rank();
+  const uint32_t csize = cluster_size();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * kRouterBT;
   const int ncols = p.noisy ? 2 * p.E : p.E;
 
-  // fused clear of the fp32 accumulator rows of these tokens (forward path)
+  // fused clear of the fp32 accumulator rows of these tokens (forward path),
+  // shared among the CTAs of the cluster
   if (p.zero_rows != nullptr) {
     const int64_t rows = (p.T - t0 < kRouterBT) ? (p.T - t0) : kRouterBT;
     float4* z = reinterpret_cast<float4*>(p.zero_rows + t0 * p.zero_width);
     const int64_t n4 = rows * p.zero_width / 4;
-    for (int64_t i = tid; i < n4; i += kRouterThreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = tid + static_cast<int64_t>(crank) * kRouterThreads; i < n4;
+         i += static_cast<int64_t>(kRouterThreads) * csize)
+      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
   float acc[TM][TN];
@@ -84,41 +222,44 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
   const TX* x = static_cast<const TX*>(p.x);
-  for (int k0 = 0; k0 < p.d; k0 += kRouterBK) {
-    // stage x^T: thread -> token tid/4, k sub-range (tid%4)*8 .. +8
-    {
-      const int tok = tid >> 2;
-      const int kk = (tid & 3) * 8;
-      const int64_t t = t0 + tok;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int kg = k0 + kk + i;
-        float v = 0.f;
-        if (t < p.T && kg < p.d) v = to_f32<TX>(x[t * p.d + kg]);
-        xs[(kk + i) * XS + tok] = v;
-      }
-    }
-    // stage W rows k0..k0+BK, columns [0, EPAD); [W_g | W_noise] when noisy
-    for (int idx = tid; idx < kRouterBK * EPAD; idx += kRouterThreads) {
-      const int r = idx / EPAD, c = idx % EPAD;
-      const int kg = k0 + r;
-      float v = 0.f;
-      if (kg < p.d && c < ncols)
-        v = (c < p.E) ? p.W_g[static_cast<int64_t>(kg) * p.E + c]
-                      : p.W_noise[static_cast<int64_t>(kg) * p.E + (c - p.E)];
-      ws[r * EPAD + c] = v;
+  const int nchunk = (p.d + kRouterBK - 1) / kRouterBK;
+  // chunks of this CTA: crank, crank + csize, ...
+  int c = static_cast<int>(crank);
+  XFrag<TX> xf;
+  if (c < nchunk) {
+    load_x_frag<TX>(xf, x, p.T, p.d, t0, c * kRouterBK, tid);
+    load_w_chunk<EPAD>(rsm + kRouterBK * kRouterXS, p, ncols, c * kRouterBK, tid);
+  }
+  cp_async_commit();
+  for (int it = 0; c < nchunk; ++it, c += csize) {
+    float* stage = rsm + (it & 1) * S::stage_floats;
+    float* xs = stage;
+    float* ws = stage + kRouterBK * kRouterXS;
+    store_x_frag<TX>(xf, xs, tid);
+    const int cn = c + static_cast<int>(csize);
+    if (cn < nchunk) {
+      float* nstage = rsm + ((it + 1) & 1) * S::stage_floats;
+      load_x_frag<TX>(xf, x, p.T, p.d, t0, cn * kRouterBK, tid);
+      load_w_chunk<EPAD>(nstage + kRouterBK * kRouterXS, p, ncols, cn * kRouterBK, tid);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-#pragma unroll 4
-    for (int kk = 0; kk < kRouterBK; ++kk) {
-      const float4 a4 = *reinterpret_cast<const float4*>(&xs[kk * XS + ty * TM]);
-      const float a[TM] = {a4.x, a4.y, a4.z, a4.w};
-      float b[TN];
 #pragma unroll
-      for (int j = 0; j < TN; j += 2) {
-        const float2 b2 = *reinterpret_cast<const float2*>(&ws[kk * EPAD + tx * TN + j]);
-        b[j] = b2.x;
-        b[j + 1] = b2.y;
+    for (int kk = ks; kk < kRouterBK; kk += S::SPLIT) {
+      float a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(xs + kk * kRouterXS + tok0 + i);
+        a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
+      }
+#pragma unroll
+      for (int j = 0; j < TN; j += 4) {
+        // column chunk j/4 of this lane: columns 8 * j + 4 * cg .. + 4
+        const float4 v = *reinterpret_cast<const float4*>(ws + kk * EPAD + 8 * j + 4 * cg);
+        b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
       }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
@@ -127,28 +268,57 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     }
     __syncthreads();
   }
+  cp_async_wait<0>();
+  __syncthreads();
 
-  // logits tile to shared memory: L[tok][col], row stride EPAD + 1
-  float* L = rsm;
+  // partial tiles of the k-phases: part[ks][token][column]
+  float* part = rsm;
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < TN; ++j) L[(ty * TM + i) * (EPAD + 1) + tx * TN + j] = acc[i][j];
+    for (int j = 0; j < TN; ++j)
+      part[(ks * kRouterBT + tok0 + i) * S::LS + 8 * (j & ~3) + 4 * cg + (j & 3)] = acc[i][j];
   __syncthreads();
+  // fixed-order sum over the phases, in place into part[0]
+  for (int idx = tid; idx < kRouterBT * EPAD; idx += kRouterThreads) {
+    const int tok = idx / EPAD, col = idx % EPAD;
+    float s = part[tok * S::LS + col];
+#pragma unroll
+    for (int q = 1; q < S::SPLIT; ++q) s += part[(q * kRouterBT + tok) * S::LS + col];
+    part[tok * S::LS + col] = s;
+  }
+  __syncthreads();
+  if (csize > 1) {
+    // the leader adds the other CTAs' tiles (ranks in order: fixed summation order)
+    cluster_sync_all();
+    if (crank == 0) {
+      const uint32_t local = smem_addr(part);
+      for (int idx = tid; idx < kRouterBT * EPAD; idx += kRouterThreads) {
+        const int tok = idx / EPAD, col = idx % EPAD;
+        const uint32_t off = (tok * S::LS + col) * 4;
+        float s = part[tok * S::LS + col];
+        for (uint32_t r = 1; r < csize; ++r) s += ld_shared_cluster_f32(mapa_shared(local + off, r));
+        part[tok * S::LS + col] = s;
+      }
+    }
+    cluster_sync_all();   // the other CTAs stay resident until the leader has read them
+    if (crank != 0) return;
+    __syncthreads();
+  }
 
   // per-token softmax + top-k: one warp per token
   constexpr int PER_LANE = EPAD / 32;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int tok = warp; tok < kRouterBT; tok += kRouterThreads / 32) {
+  const float* L = part;
+  for (int tok = warp; tok < kRouterBT; tok += kRouterWarps) {
     const int64_t t = t0 + tok;
     if (t >= p.T) break;
-    const float* Lr = L + tok * (EPAD + 1);
+    const float* Lr = L + tok * S::LS;
     float lg[PER_LANE], key[PER_LANE], sv[PER_LANE];
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-      const int c = lane + 32 * i;
-      lg[i] = (c < p.E) ? Lr[c] : -INFINITY;
+      const int cc = lane + 32 * i;
+      lg[i] = (cc < p.E) ? Lr[cc] : -INFINITY;
       m = fmaxf(m, lg[i]);
     }
 #pragma unroll
@@ -156,8 +326,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     float ssum = 0.f;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-      const int c = lane + 32 * i;
-      sv[i] = (c < p.E) ? expf(lg[i] - m) : 0.f;
+      const int cc = lane + 32 * i;
+      sv[i] = (cc < p.E) ? expf(lg[i] - m) : 0.f;
       ssum += sv[i];
     }
 #pragma unroll
@@ -165,19 +335,19 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
     const float inv = 1.0f / ssum;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-      const int c = lane + 32 * i;
+      const int cc = lane + 32 * i;
       sv[i] *= inv;
-      if (c >= p.E) {
+      if (cc >= p.E) {
         key[i] = -INFINITY;
       } else if (p.noisy) {
-        key[i] = lg[i] + p.eps[t * p.E + c] * softplus_f(Lr[p.E + c]);
+        key[i] = lg[i] + p.eps[t * p.E + cc] * softplus_f(Lr[p.E + cc]);
       } else if (p.bias != nullptr) {
-        key[i] = sv[i] + p.bias[c];
+        key[i] = sv[i] + p.bias[cc];
       } else {
         key[i] = lg[i];   // Softmax is increasing: the order of s is the order of the logits
       }
       if (key[i] != key[i]) key[i] = -INFINITY;   // a NaN key ranks last, ids stay valid
-      if (p.logits_out != nullptr && c < p.E) p.logits_out[t * p.E + c] = lg[i];
+      if (p.logits_out != nullptr && cc < p.E) p.logits_out[t * p.E + cc] = lg[i];
     }
 
     uint32_t taken = 0;
@@ -189,10 +359,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterArgs
       int ib = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < PER_LANE; ++i) {
-        const int c = lane + 32 * i;
-        if (c < p.E && !((taken >> i) & 1u) && better(key[i], c, kb, ib)) {
+        const int cc = lane + 32 * i;
+        if (cc < p.E && !((taken >> i) & 1u) && better(key[i], cc, kb, ib)) {
           kb = key[i];
-          ib = c;
+          ib = cc;
           vb = p.noisy ? key[i] : sv[i];
         }
       }
