@@ -242,7 +242,7 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   if (nblk == 0) return MOE_OK;
   // Few token blocks (decode-sized T): a cluster of CS CTAs also splits the
   // k-chunks, until there are about two CTAs per SM or two chunks per CTA.
-  const int nchunk = (c->d + kRouterBK - 1) / kRouterBK;
+  const int nchunk = (c->d + 63) / 64;   // the smallest k-chunk of any router shape
   int cs = 1;
   while (cs < 8 && nblk * cs < 2ll * sm_count && nchunk >= 4 * cs) cs *= 2;
   cudaLaunchConfig_t lc{};

@@ -43,25 +43,30 @@ struct RouterArgs {
 };
 
 constexpr int kRouterBT = 32;       // tokens per CTA
-constexpr int kRouterBK = 64;       // k-chunk staged in shared memory
 constexpr int kRouterThreads = 256;
 constexpr int kRouterWarps = kRouterThreads / 32;
-constexpr int kRouterXS = kRouterBT + 4;   // row stride of the staged x^T chunk
 
+// Fixed for any column count of the kernel: the token block. Per column
+// count: the k-chunk BK and the register tile.
 template <int EPAD>
 struct RouterShape {
+  static constexpr int BT = kRouterBT;
+  static constexpr int BK = 64;                  // k-chunk staged in shared memory
+  static constexpr int XS = BT + 4;              // row stride of the staged x^T chunk
   static constexpr int TN = EPAD / 8;            // columns per thread (8 column groups per warp)
   static constexpr int TM = EPAD <= 64 ? 8 : 4;  // tokens per thread (4 token groups per warp)
   static constexpr int WT = 4 * TM;              // tokens per warp tile
-  static constexpr int WROWS = kRouterBT / WT;   // warp rows covering the CTA's tokens
+  static constexpr int WROWS = BT / WT;          // warp rows covering the CTA's tokens
   static constexpr int SPLIT = kRouterWarps / WROWS;   // warps sharing one k-chunk
   static constexpr int LS = EPAD + 1;            // row stride of the logits tiles
-  static constexpr size_t stage_floats = kRouterBK * kRouterXS + kRouterBK * EPAD;
-  static constexpr size_t part_floats = static_cast<size_t>(SPLIT) * kRouterBT * LS;
+  static constexpr int XVEC = BT * BK / 8 / kRouterThreads;   // x vectors per thread per chunk
+  static constexpr size_t stage_floats = BK * XS + BK * EPAD;
+  static constexpr size_t part_floats = static_cast<size_t>(SPLIT) * BT * LS;
   static constexpr size_t smem_bytes =
       (2 * stage_floats > part_floats ? 2 * stage_floats : part_floats) * sizeof(float);
-  static_assert(WROWS * WT == kRouterBT && SPLIT * WROWS == kRouterWarps, "router tiling");
-  static_assert(kRouterBK % SPLIT == 0 && TN % 4 == 0 && TM % 4 == 0, "router tiling");
+  static_assert(WROWS * WT == BT && SPLIT * WROWS == kRouterWarps, "router tiling");
+  static_assert(BK % SPLIT == 0 && TN % 4 == 0 && TM % 4 == 0, "router tiling");
+  static_assert(XVEC * 8 * kRouterThreads == BT * BK && BT % 32 == 0, "router x staging");
 };
 
 template <int EPAD>
@@ -112,78 +117,166 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   return v;
 }
 
-// x chunk [BT tokens][BK] -> registers: thread -> token tid % 32, k sub-range
-// (tid / 32) * 8 .. + 8 (one 16-byte load for bf16, two for fp32). Kept raw
-// until the store so the prefetch costs as few registers as possible.
-template <typename TX>
-struct XFrag {
-  uint4 u[sizeof(TX) / 2];
+// x chunk [BT tokens][BK] -> registers, in 8-element vectors: vector
+// v = tid + 256 i covers token v % BT, k sub-range (v / BT) * 8 .. + 8 (one
+// 16-byte load for bf16, two for fp32). Consecutive lanes take consecutive
+// tokens, so the transposed shared-memory stores are conflict-free. Kept raw
+// until the store so the prefetch costs as few registers as possible. The
+// per-thread row pointers are computed once per kernel.
+template <typename TX, typename S>
+struct XStager {
+  const TX* src[S::XVEC];   // x row of the vector's token at its k sub-range offset
+  bool ok[S::XVEC];         // token < T
+  uint4 u[S::XVEC][sizeof(TX) / 2];
+
+  __device__ __forceinline__ void init(const TX* x, int64_t T, int32_t d, int64_t t0, int tid) {
+#pragma unroll
+    for (int v = 0; v < S::XVEC; ++v) {
+      const int vi = tid + v * kRouterThreads;
+      const int64_t t = t0 + vi % S::BT;
+      ok[v] = t < T;
+      src[v] = x + (ok[v] ? t : 0) * d + (vi / S::BT) * 8;
+    }
+  }
+  __device__ __forceinline__ void load(int k0, int32_t d, int tid) {
+#pragma unroll
+    for (int v = 0; v < S::XVEC; ++v) {
+      const int kg = k0 + ((tid + v * kRouterThreads) / S::BT) * 8;
+      const bool in = ok[v] && kg < d;   // d % 8 == 0: a vector is entirely in or out
+#pragma unroll
+      for (int i = 0; i < static_cast<int>(sizeof(TX) / 2); ++i)
+        u[v][i] = in ? __ldg(reinterpret_cast<const uint4*>(src[v] + k0) + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  __device__ __forceinline__ void store(float* xs, int tid) const {
+#pragma unroll
+    for (int v = 0; v < S::XVEC; ++v) {
+      const int vi = tid + v * kRouterThreads;
+      const int tok = vi % S::BT;
+      const int kk = (vi / S::BT) * 8;
+      float w[8];
+      if constexpr (sizeof(TX) == 2) {
+        const uint32_t r[4] = {u[v][0].x, u[v][0].y, u[v][0].z, u[v][0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // bf16 -> fp32 is exact: the bf16 bits are the high half
+          w[2 * i] = __uint_as_float(r[i] << 16);
+          w[2 * i + 1] = __uint_as_float(r[i] & 0xffff0000u);
+        }
+      } else {
+        const uint32_t r[8] = {u[v][0].x, u[v][0].y, u[v][0].z, u[v][0].w,
+                               u[v][1].x, u[v][1].y, u[v][1].z, u[v][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = __uint_as_float(r[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[(kk + i) * S::XS + tok] = w[i];
+    }
+  }
 };
 
-template <typename TX>
-__device__ __forceinline__ void load_x_frag(XFrag<TX>& f, const TX* x, int64_t T, int32_t d,
-                                            int64_t t0, int k0, int tid) {
-  const int64_t t = t0 + (tid & 31);
-  const int kg = k0 + (tid >> 5) * 8;
-  const bool ok = t < T && kg < d;   // d % 8 == 0: a vector is entirely in or out
-#pragma unroll
-  for (int i = 0; i < static_cast<int>(sizeof(TX) / 2); ++i)
-    f.u[i] = ok ? __ldg(reinterpret_cast<const uint4*>(x + t * d + kg) + i) : make_uint4(0u, 0u, 0u, 0u);
-}
+// W chunk rows k0..k0+BK, columns [0, EPAD) of [W_g | W_noise] -> ws, async,
+// in pieces of VW floats (4 when every piece is 16-byte aligned, else 1).
+// Piece idx = tid + 256 n covers column (idx % (EPAD/VW)) * VW, which is the
+// same for every n, and row idx / (EPAD/VW); the column's source pointer is
+// computed once per kernel.
+template <int EPAD, int BK, int VW>
+struct WStager {
+  static constexpr int V = EPAD / VW;           // pieces per row
+  static constexpr int RS = kRouterThreads / V; // row step between a thread's pieces
+  static constexpr int NV = BK / RS;            // pieces per thread per chunk
+  static_assert(RS * V == kRouterThreads && NV * RS == BK, "router W staging");
+  const float* col_src;   // column base in W_g or W_noise
+  int32_t E, d, r0;
+  bool col_ok;
+  uint32_t dst0;          // byte offset of the thread's first piece inside a stage's W tile
 
-template <typename TX>
-__device__ __forceinline__ void store_x_frag(const XFrag<TX>& f, float* xs, int tid) {
-  const int tok = tid & 31;
-  const int kk = (tid >> 5) * 8;
-  float v[8];
-  if constexpr (sizeof(TX) == 2) {
-    const uint32_t w[4] = {f.u[0].x, f.u[0].y, f.u[0].z, f.u[0].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {   // bf16 -> fp32 is exact: the bf16 bits are the high half
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  } else {
-    const uint32_t w[8] = {f.u[0].x, f.u[0].y, f.u[0].z, f.u[0].w, f.u[1].x, f.u[1].y, f.u[1].z, f.u[1].w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(w[i]);
+  __device__ __forceinline__ void init(const RouterArgs& p, int ncols, int tid) {
+    const int c = (tid % V) * VW;
+    r0 = tid / V;
+    E = p.E;
+    d = p.d;
+    col_ok = c < ncols;
+    col_src = (c < p.E) ? p.W_g + c : p.W_noise + (c - p.E);
+    if (!col_ok) col_src = p.W_g;
+    dst0 = (r0 * EPAD + c) * 4;
   }
+  __device__ __forceinline__ void load(uint32_t ws_base, int k0) const {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) xs[(kk + i) * kRouterXS + tok] = v[i];
-}
-
-// W chunk rows k0..k0+BK, columns [0, EPAD) of [W_g | W_noise] -> ws, async.
-template <int EPAD>
-__device__ __forceinline__ void load_w_chunk(float* ws, const RouterArgs& p, int ncols, int k0, int tid) {
-  const uint32_t base = smem_addr(ws);
-  if (p.w_vec4) {
-    constexpr int V = EPAD / 4;
-    for (int idx = tid; idx < kRouterBK * V; idx += kRouterThreads) {
-      const int r = idx / V, c = (idx % V) * 4;
-      const int kg = k0 + r;
-      const float* src = p.W_g;
-      uint32_t n = 0;
-      if (kg < p.d && c < ncols) {
-        src = (c < p.E) ? p.W_g + static_cast<int64_t>(kg) * p.E + c
-                        : p.W_noise + static_cast<int64_t>(kg) * p.E + (c - p.E);
-        n = 16;
-      }
-      cp_async16(base + (r * EPAD + c) * 4, src, n);
-    }
-  } else {
-    for (int idx = tid; idx < kRouterBK * EPAD; idx += kRouterThreads) {
-      const int r = idx / EPAD, c = idx % EPAD;
-      const int kg = k0 + r;
-      const float* src = p.W_g;
-      uint32_t n = 0;
-      if (kg < p.d && c < ncols) {
-        src = (c < p.E) ? p.W_g + static_cast<int64_t>(kg) * p.E + c
-                        : p.W_noise + static_cast<int64_t>(kg) * p.E + (c - p.E);
-        n = 4;
-      }
-      cp_async4(base + idx * 4, src, n);
+    for (int n = 0; n < NV; ++n) {
+      const int kg = k0 + r0 + n * RS;
+      const bool in = col_ok && kg < d;
+      const float* src = in ? col_src + static_cast<int64_t>(kg) * E : col_src;
+      if constexpr (VW == 4)
+        cp_async16(ws_base + dst0 + n * RS * EPAD * 4, src, in ? 16u : 0u);
+      else
+        cp_async4(ws_base + dst0 + n * RS * EPAD * 4, src, in ? 4u : 0u);
     }
   }
+};
+
+// The k-loop of the router GEMM: acc[i][j] += x[tok0 + i, k] * W[k, col(j)]
+// over the chunks crank, crank + csize, ... of this CTA.
+template <typename TX, int EPAD, int VW>
+__device__ __forceinline__ void router_mainloop(const RouterArgs& p, float* rsm, int64_t t0,
+                                                int crank, int csize, int tid, int tok0, int ks,
+                                                int cg, float (&acc)[RouterShape<EPAD>::TM][RouterShape<EPAD>::TN]) {
+  using S = RouterShape<EPAD>;
+  constexpr int TM = S::TM, TN = S::TN;
+  const int ncols = p.noisy ? 2 * p.E : p.E;
+  const int nchunk = (p.d + S::BK - 1) / S::BK;
+  XStager<TX, S> xst;
+  xst.init(static_cast<const TX*>(p.x), p.T, p.d, t0, tid);
+  WStager<EPAD, S::BK, VW> wst;
+  wst.init(p, ncols, tid);
+  const uint32_t smem0 = smem_addr(rsm);
+  constexpr uint32_t kWOff = S::BK * S::XS * 4;      // W tile offset inside a stage (bytes)
+  constexpr uint32_t kStageB = S::stage_floats * 4;  // stage size (bytes)
+
+  int c = crank;
+  if (c < nchunk) {
+    xst.load(c * S::BK, p.d, tid);
+    wst.load(smem0 + kWOff, c * S::BK);
+  }
+  cp_async_commit();
+  for (int it = 0; c < nchunk; ++it, c += csize) {
+    float* xs = rsm + (it & 1) * S::stage_floats;
+    const float* ws = xs + S::BK * S::XS;
+    xst.store(xs, tid);
+    const int cn = c + csize;
+    if (cn < nchunk) {
+      xst.load(cn * S::BK, p.d, tid);
+      wst.load(smem0 + ((it + 1) & 1) * kStageB + kWOff, cn * S::BK);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const float* xa = xs + ks * S::XS + tok0;
+    const float* wb = ws + ks * EPAD + 4 * cg;
+#pragma unroll
+    for (int step = 0; step < S::BK / S::SPLIT; ++step) {
+      float a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(xa + step * S::SPLIT * S::XS + i);
+        a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
+      }
+#pragma unroll
+      for (int j = 0; j < TN; j += 4) {
+        // column chunk j/4 of this lane: columns 8 * j + 4 * cg .. + 4
+        const float4 v = *reinterpret_cast<const float4*>(wb + step * S::SPLIT * EPAD + 8 * j);
+        b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
 }
 
 template <typename TX, int EPAD>
@@ -201,13 +294,12 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
 
   const uint32_t crank = cluster_rank();
   const uint32_t csize = cluster_size();
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * kRouterBT;
-  const int ncols = p.noisy ? 2 * p.E : p.E;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * S::BT;
 
   // fused clear of the fp32 accumulator rows of these tokens (forward path),
   // shared among the CTAs of the cluster
   if (p.zero_rows != nullptr) {
-    const int64_t rows = (p.T - t0 < kRouterBT) ? (p.T - t0) : kRouterBT;
+    const int64_t rows = (p.T - t0 < S::BT) ? (p.T - t0) : S::BT;
     float4* z = reinterpret_cast<float4*>(p.zero_rows + t0 * p.zero_width);
     const int64_t n4 = rows * p.zero_width / 4;
     for (int64_t i = tid + static_cast<int64_t>(crank) * kRouterThreads; i < n4;
@@ -221,55 +313,10 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-  const TX* x = static_cast<const TX*>(p.x);
-  const int nchunk = (p.d + kRouterBK - 1) / kRouterBK;
-  // chunks of this CTA: crank, crank + csize, ...
-  int c = static_cast<int>(crank);
-  XFrag<TX> xf;
-  if (c < nchunk) {
-    load_x_frag<TX>(xf, x, p.T, p.d, t0, c * kRouterBK, tid);
-    load_w_chunk<EPAD>(rsm + kRouterBK * kRouterXS, p, ncols, c * kRouterBK, tid);
-  }
-  cp_async_commit();
-  for (int it = 0; c < nchunk; ++it, c += csize) {
-    float* stage = rsm + (it & 1) * S::stage_floats;
-    float* xs = stage;
-    float* ws = stage + kRouterBK * kRouterXS;
-    store_x_frag<TX>(xf, xs, tid);
-    const int cn = c + static_cast<int>(csize);
-    if (cn < nchunk) {
-      float* nstage = rsm + ((it + 1) & 1) * S::stage_floats;
-      load_x_frag<TX>(xf, x, p.T, p.d, t0, cn * kRouterBK, tid);
-      load_w_chunk<EPAD>(nstage + kRouterBK * kRouterXS, p, ncols, cn * kRouterBK, tid);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = ks; kk < kRouterBK; kk += S::SPLIT) {
-      float a[TM], b[TN];
-#pragma unroll
-      for (int i = 0; i < TM; i += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(xs + kk * kRouterXS + tok0 + i);
-        a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
-      }
-#pragma unroll
-      for (int j = 0; j < TN; j += 4) {
-        // column chunk j/4 of this lane: columns 8 * j + 4 * cg .. + 4
-        const float4 v = *reinterpret_cast<const float4*>(ws + kk * EPAD + 8 * j + 4 * cg);
-        b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
-      }
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-  cp_async_wait<0>();
-  __syncthreads();
+  if (p.w_vec4)
+    router_mainloop<TX, EPAD, 4>(p, rsm, t0, crank, csize, tid, tok0, ks, cg, acc);
+  else
+    router_mainloop<TX, EPAD, 1>(p, rsm, t0, crank, csize, tid, tok0, ks, cg, acc);
 
   // partial tiles of the k-phases: part[ks][token][column]
   float* part = rsm;
@@ -277,14 +324,14 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
   for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < TN; ++j)
-      part[(ks * kRouterBT + tok0 + i) * S::LS + 8 * (j & ~3) + 4 * cg + (j & 3)] = acc[i][j];
+      part[(ks * S::BT + tok0 + i) * S::LS + 8 * (j & ~3) + 4 * cg + (j & 3)] = acc[i][j];
   __syncthreads();
   // fixed-order sum over the phases, in place into part[0]
-  for (int idx = tid; idx < kRouterBT * EPAD; idx += kRouterThreads) {
+  for (int idx = tid; idx < S::BT * EPAD; idx += kRouterThreads) {
     const int tok = idx / EPAD, col = idx % EPAD;
     float s = part[tok * S::LS + col];
 #pragma unroll
-    for (int q = 1; q < S::SPLIT; ++q) s += part[(q * kRouterBT + tok) * S::LS + col];
+    for (int q = 1; q < S::SPLIT; ++q) s += part[(q * S::BT + tok) * S::LS + col];
     part[tok * S::LS + col] = s;
   }
   __syncthreads();
@@ -293,7 +340,7 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
     cluster_sync_all();
     if (crank == 0) {
       const uint32_t local = smem_addr(part);
-      for (int idx = tid; idx < kRouterBT * EPAD; idx += kRouterThreads) {
+      for (int idx = tid; idx < S::BT * EPAD; idx += kRouterThreads) {
         const int tok = idx / EPAD, col = idx % EPAD;
         const uint32_t off = (tok * S::LS + col) * 4;
         float s = part[tok * S::LS + col];
@@ -309,7 +356,7 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
   // per-token softmax + top-k: one warp per token
   constexpr int PER_LANE = EPAD / 32;
   const float* L = part;
-  for (int tok = warp; tok < kRouterBT; tok += kRouterWarps) {
+  for (int tok = warp; tok < S::BT; tok += kRouterWarps) {
     const int64_t t = t0 + tok;
     if (t >= p.T) break;
     const float* Lr = L + tok * S::LS;
