@@ -165,24 +165,27 @@ def cpu_oracle_rate(w, inp, budget_s: float) -> dict:
 
 
 def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
-    """Per-step time of the public API with pinned-host x (and eps) copied in and
-    y copied out inside the timed region."""
-    x_host = inp["x"].pin_memory()
-    eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
-    y_host = torch.empty(tuple(layer.y.shape), dtype=layer.y.dtype, pin_memory=True)
-    x_dev = torch.empty_like(x)
-    eps_dev = torch.empty_like(eps) if eps is not None else None
-    for _ in range(args.warmup):
-        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
+    """Per-step time of the public API over host batches: every step copies its
+    x (and eps) in from pinned host memory and its y back out, inside the timed
+    region; the copies of neighbouring steps overlap the forward
+    (MoELayer.forward_host_stream)."""
+    n = args.steps
+    x_hosts = [inp["x"].pin_memory() for _ in range(2)]
+    eps_hosts = [inp["eps"].pin_memory() for _ in range(2)] if inp["eps"] is not None else None
+    y_hosts = [torch.empty(tuple(layer.y.shape), dtype=layer.y.dtype, pin_memory=True) for _ in range(2)]
+
+    def run(k):
+        xs = [x_hosts[i & 1] for i in range(k)]
+        es = [eps_hosts[i & 1] for i in range(k)] if eps_hosts is not None else None
+        return layer.forward_host_stream(xs, [y_hosts[i & 1] for i in range(k)], es)
+
+    run(max(args.warmup, 2))
     barrier()
     e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for _ in range(args.steps):
-        layer.forward_host(x_host, eps_host, y_host, x_dev, eps_dev)
-    e_end.record(stream)
+    e_end = run(n)
     barrier()
-    ms = e_start.elapsed_time(e_end) / args.steps
+    ms = e_start.elapsed_time(e_end) / n
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)

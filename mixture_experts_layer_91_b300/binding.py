@@ -276,7 +276,8 @@ class MoELayer:
 
     __call__(x, eps) runs on device tensors; forward_host(x_host, eps_host)
     copies the step's inputs from pinned host memory, runs the layer and
-    copies y back, all on the current stream.
+    copies y back, all on the current stream; forward_host_stream runs a
+    sequence of host batches with the copies overlapping the forwards.
     """
 
     def __init__(self, w: Workload, inputs: dict, device="cuda"):
@@ -292,6 +293,8 @@ class MoELayer:
         self.workspace = _workspace(workspace_size(self.cfg), dev)
         self.y = torch.empty(w.T, w.d, dtype=act_dtype(self.cfg), device=dev)
         self.device = dev
+        self._streams = {}
+        self._bufs = {}
 
     def __call__(self, x, eps=None, y=None):
         return forward(self.cfg, x, self.W_g, self.W_noise, eps, self.bias, self.W1, self.W3, self.W2,
@@ -300,6 +303,57 @@ class MoELayer:
     def profiled(self, x, events, eps=None):
         return forward_profiled(self.cfg, x, self.W_g, self.W_noise, eps, self.bias, self.W1, self.W3,
                                 self.W2, workspace=self.workspace, y=self.y, events=events)
+
+    def forward_host_stream(self, x_hosts, y_hosts, eps_hosts=None):
+        """Run the layer over a sequence of batches held in pinned host memory.
+
+        Batch i is copied in on an upload stream, computed on the current
+        stream and copied back into y_hosts[i] on a download stream, with two
+        device buffers for x and y, so the copies of batches i+1 and i-1
+        overlap the forward of batch i. Every copy is enqueued before this
+        returns; synchronise the current stream (or the returned event) to
+        read y_hosts. Returns the CUDA event recorded after the last copy-back.
+        """
+        n = len(x_hosts)
+        if len(y_hosts) != n or (eps_hosts is not None and len(eps_hosts) != n):
+            raise ValueError("one output (and eps) buffer per input batch")
+        comp = torch.cuda.current_stream(self.device)
+        up = self._streams.setdefault("up", torch.cuda.Stream(self.device))
+        down = self._streams.setdefault("down", torch.cuda.Stream(self.device))
+        if "x" not in self._bufs:
+            self._bufs["x"] = [torch.empty_like(x_hosts[0], device=self.device) for _ in range(2)]
+            self._bufs["y"] = [torch.empty_like(self.y) for _ in range(2)]
+            if eps_hosts is not None:
+                self._bufs["eps"] = [torch.empty_like(eps_hosts[0], device=self.device) for _ in range(2)]
+        xb, yb, eb = self._bufs["x"], self._bufs["y"], self._bufs.get("eps")
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        downloaded = [torch.cuda.Event() for _ in range(2)]
+        up.wait_stream(comp)      # buffers may still be read by earlier work on `comp`
+        down.wait_stream(comp)
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(computed[b])          # forward i-2 has read xb[b]
+                xb[b].copy_(x_hosts[i], non_blocking=True)
+                if eb is not None:
+                    eb[b].copy_(eps_hosts[i], non_blocking=True)
+                uploaded[b].record(up)
+            comp.wait_event(uploaded[b])
+            if i >= 2:
+                comp.wait_event(downloaded[b])          # copy-back i-2 has read yb[b]
+            self(xb[b], eb[b] if eb is not None else None, y=yb[b])
+            computed[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[b])
+                y_hosts[i].copy_(yb[b], non_blocking=True)
+                downloaded[b].record(down)
+        comp.wait_stream(down)
+        comp.wait_stream(up)
+        done = torch.cuda.Event(enable_timing=True)
+        done.record(comp)
+        return done
 
     def forward_host(self, x_host, eps_host=None, y_host=None, x_dev=None, eps_dev=None):
         x_dev = x_dev if x_dev is not None else torch.empty_like(x_host, device=self.device)

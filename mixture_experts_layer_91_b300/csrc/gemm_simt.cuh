@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kSimtThreads) grouped_gemm_simt(const SimtArgs
   for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
     const int32_t sub = static_cast<int32_t>(t / n_tiles);
     const int32_t nt = static_cast<int32_t>(t % n_tiles);
-    const TileCoord c = decode_tile(sub / (kTcBM / kSimtBM), 1, p.plan.mt_start, p.G);
+    const TileCoord c = decode_tile(sub / (kTcBM / kSimtBM), 1, p.plan.mt_start, p.G, p.n_shared, 0, 0);
     const int32_t s4 = sub % (kTcBM / kSimtBM);
     const int32_t row0 = c.lmt * kTcBM + s4 * kSimtBM;    // first row within the group
     const int32_t gsz = __ldg(p.plan.gsize + c.g);

@@ -74,6 +74,7 @@ struct TcArgs {
   const int32_t* perm_src;  // down scatter: flat assignment index of grouped rows
   const float* topk_w;      // down scatter: gate values [T*k]
   int32_t top_k;
+  int32_t fold_mt;          // down scatter with K_s > 0: m-tiles per shared group, else 0
 };
 
 struct TcMaps {
@@ -93,13 +94,33 @@ constexpr size_t tc_smem_bytes(int mode) {
 
 struct TileCoord {
   int32_t g, lmt, mt, nt;
+  int32_t nk;   // k-blocks of the tile's reduction
 };
 
+// Tile t -> (group, m-tile, n-tile). With fold_mt > 0 (the down projection
+// feeding the gate-weighted combine) the K_s shared experts are folded into
+// one group whose reduction runs over all K_s * I intermediate columns: every
+// shared expert has gate 1 and the same input rows, so
+//   sum_i W2_i h_i = [W2_0 | ... | W2_{K_s-1}] [h_0; ...; h_{K_s-1}],
+// the fine-grained segmentation identity read backwards (DeepSeekMoE
+// translation, section 3.1). Its tiles are the first fold_mt m-tiles; the
+// m-tiles of shared groups 1..K_s-1 are skipped.
 __device__ __forceinline__ TileCoord decode_tile(int32_t t, int32_t n_tiles, const int32_t* mt_start,
-                                                 int32_t G) {
+                                                 int32_t G, int32_t n_shared, int32_t fold_mt,
+                                                 int32_t nk) {
   TileCoord c;
   c.mt = t / n_tiles;
   c.nt = t - c.mt * n_tiles;
+  c.nk = nk;
+  if (fold_mt > 0) {
+    if (c.mt < fold_mt) {
+      c.g = 0;
+      c.lmt = c.mt;
+      c.nk = n_shared * nk;
+      return c;
+    }
+    c.mt += (n_shared - 1) * fold_mt;
+  }
   int lo = 0, hi = G;  // largest g with mt_start[g] <= mt (skips empty groups)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -166,8 +187,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int32_t total = __ldg(p.plan.mt_start + p.G) * p.n_tiles;
-  const int32_t nk = (p.K + kTcBK - 1) / kTcBK;
+  const int32_t folded = p.fold_mt > 0 ? (p.n_shared - 1) * p.fold_mt : 0;
+  const int32_t total = (__ldg(p.plan.mt_start + p.G) - folded) * p.n_tiles;
+  const int32_t nk = (p.K + kTcBK - 1) / kTcBK;   // k-blocks per expert
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -175,7 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileCoord c = decode_tile(t, p.n_tiles, p.plan.mt_start, p.G);
+        const TileCoord c = decode_tile(t, p.n_tiles, p.plan.mt_start, p.G, p.n_shared, p.fold_mt, nk);
         const CUtensorMap* amap = &maps.a0;
         int32_t a_y;
         if (MODE == kEpiSwiGLU) {
@@ -185,7 +207,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           a_y = c.mt * kTcBM;   // padded H row of this m-tile
         }
         const int32_t b_y = c.g * p.b_rows + c.nt * (MODE == kEpiSwiGLU ? kTcBN / 2 : kTcBN);
-        for (int32_t kb = 0; kb < nk; ++kb, ++it) {
+        for (int32_t kb = 0, e = 0, kx = 0; kb < c.nk; ++kb, ++it) {
+          // folded shared group: k-block kb is block kx of shared expert e
+          if (kx == nk) { kx = 0; ++e; }
           const uint32_t s = it % kTcStages;
           const uint32_t ph = (it / kTcStages) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort)) { ok = false; break; }
@@ -193,13 +217,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(full, kStageBytes);
           const uint32_t sa = sA0 + s * kStageBytes;
           const uint32_t sb = sB0 + s * kStageBytes;
-          tma_load_2d(sa, amap, full, kb * kTcBK, a_y);
           if (MODE == kEpiSwiGLU) {
+            tma_load_2d(sa, amap, full, kb * kTcBK, a_y);
             tma_load_2d(sb, &maps.b0, full, kb * kTcBK, b_y);
             tma_load_2d(sb + kTileBBytes / 2, &maps.b1, full, kb * kTcBK, b_y);
           } else {
-            tma_load_2d(sb, &maps.b0, full, kb * kTcBK, b_y);
+            // expert e's H rows start at its own m-tiles; its W2 rows at e * d
+            tma_load_2d(sa, amap, full, kx * kTcBK, a_y + e * p.fold_mt * kTcBM);
+            tma_load_2d(sb, &maps.b0, full, kx * kTcBK, b_y + e * p.b_rows);
           }
+          ++kx;
         }
       }
       if (!ok) {
@@ -223,7 +250,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(bar_tempty + 8 * b, aph ^ 1u, abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kTcBN;
-        for (int32_t kb = 0; kb < nk; ++kb, ++it) {
+        const bool fused = p.fold_mt > 0 && t / p.n_tiles < p.fold_mt;   // folded shared group
+        const int32_t tile_nk = fused ? p.n_shared * nk : nk;
+        for (int32_t kb = 0; kb < tile_nk; ++kb, ++it) {
           const uint32_t s = it % kTcStages;
           const uint32_t ph = (it / kTcStages) & 1u;
           if (!mbar_wait(bar_full + 8 * s, ph, abort)) { ok = false; break; }
@@ -249,7 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     uint32_t local = 0, nstore = 0;
     for (int32_t t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-      const TileCoord c = decode_tile(t, p.n_tiles, p.plan.mt_start, p.G);
+      const TileCoord c = decode_tile(t, p.n_tiles, p.plan.mt_start, p.G, p.n_shared, p.fold_mt, nk);
       const uint32_t b = local & 1u;
       const uint32_t aph = (local >> 1) & 1u;
       const int32_t row_local = c.lmt * kTcBM + q * 32 + lane;

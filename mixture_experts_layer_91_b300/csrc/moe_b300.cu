@@ -354,6 +354,8 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.b_rows = d;
     a.n_out = d;
     a.out = out;
+    // the combine folds the shared experts into one group (gate 1 for all)
+    a.fold_mt = (mode == kEpiScatterAdd && c->n_shared > 0) ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
     if (mode == kEpiScatterAdd)
       grouped_gemm_tc<kEpiScatterAdd><<<grid, kTcThreads, tc_smem_bytes(kEpiScatterAdd), st>>>(dn, a);
     else

@@ -257,6 +257,22 @@ def test_forward_is_repeatable(cuda_lib):
     assert (y1 - y2).abs().max().item() <= 1e-2 * y1.abs().max().item()
 
 
+def test_host_stream_matches_device_forward(cuda_lib):
+    """Overlapped host-batch pipeline: each y equals the device forward of its x."""
+    w = workloads.GSHARD_NOISY.with_tokens(512)
+    inp = get_inputs(w)
+    layer = binding.MoELayer(w, inp)
+    g = torch.Generator().manual_seed(5)
+    xs = [torch.randn(w.T, w.d, generator=g).to(torch.bfloat16).pin_memory() for _ in range(5)]
+    es = [torch.randn(w.T, w.n_routed, generator=g).pin_memory() for _ in range(5)]
+    ys = [torch.empty(w.T, w.d, dtype=torch.bfloat16, pin_memory=True) for _ in range(5)]
+    layer.forward_host_stream(xs, ys, es)
+    torch.cuda.synchronize()
+    for i in range(5):
+        ref = layer(xs[i].to(DEV), es[i].to(DEV)).float().cpu().numpy()
+        check_close(ys[i].float().numpy(), ref, False, f"host batch {i}")
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     binding.debug_wait_timeout(100000)           # 0.1 s wait that nothing satisfies
     st, raw = binding.device_status()
