@@ -82,6 +82,11 @@ const char* moe_status_string(int status);
 /* Library ABI version: (major << 16) | minor. */
 int moe_version(void);
 
+/* Bytes of scratch moe_route needs: the three bf16 planes of the router
+ * weights read by the tensor-core router (0 for fp32 tokens or more than 128
+ * router columns, where the CUDA-core router runs). */
+size_t moe_route_workspace_size(const moe_config* cfg);
+
 /*
  * moe_route -- the gate: router GEMM, softmax, top-k and gate values.
  * DeepSeekMoE translation, section 3.2, eqs (10)-(11); noisy variant per the
@@ -97,11 +102,18 @@ int moe_version(void);
  *                                    ties to the lowest index
  *   topk_w   [T, k]   fp32   (out)   gate values g_{i,t} of those experts
  *   logits   [T, N_r] fp32 or NULL (out) the plain logits x W_g
- * Arithmetic is fp32 throughout (logits accumulated in fp32 FMA).
+ *   workspace, ws_bytes              scratch, >= moe_route_workspace_size()
+ *                                    (may be NULL when that is 0)
+ * The logits are an fp32-accurate dot product of the stored inputs. bf16
+ * tokens with at most 128 router columns (N_r, or 2 N_r when noisy) run on
+ * the tensor cores: W is split exactly into three bf16 planes, every
+ * product is exact, and the accumulation is fp32. Otherwise a CUDA-core fp32
+ * FMA kernel runs. Softmax, keys and gates are fp32.
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g,
                      const float* W_noise, const float* eps, const float* bias,
-                     int32_t* topk_ids, float* topk_w, float* logits, void* stream);
+                     int32_t* topk_ids, float* topk_w, float* logits,
+                     void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of scratch moe_permute needs (per-block histograms and ranks). */
 size_t moe_permute_workspace_size(const moe_config* cfg);

@@ -30,7 +30,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 PERMUTE_STATIC_MAX_ASSIGN = 1 << 19   # MOE_PERMUTE_STATIC_MAX_ASSIGN
 
 # every symbol include/moe_b300.h declares
-EXPORTS = ["moe_status_string", "moe_version", "moe_route", "moe_permute_workspace_size",
+EXPORTS = ["moe_status_string", "moe_version", "moe_route_workspace_size", "moe_route",
+           "moe_permute_workspace_size",
            "moe_permute", "moe_permute_static", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_workspace_size", "moe_forward", "moe_forward_profiled", "moe_device_status",
            "moe_debug_wait_timeout"]
@@ -71,7 +72,8 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         sig = {
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "moe_version": (ctypes.c_int, []),
-            "moe_route": (I32, [C, P, P, P, P, P, P, P, P, P]),
+            "moe_route_workspace_size": (SZ, [C]),
+            "moe_route": (I32, [C, P, P, P, P, P, P, P, P, P, SZ, P]),
             "moe_permute_workspace_size": (SZ, [C]),
             "moe_permute": (I32, [C, P, P, P, SZ, P, P, P, P, P, P]),
             "moe_permute_static": (I32, [C, P, P, P, P, P, P, P, P]),
@@ -126,6 +128,10 @@ def workspace_size(cfg: MoeConfig) -> int:
     return load().moe_workspace_size(ctypes.byref(cfg))
 
 
+def route_workspace_size(cfg: MoeConfig) -> int:
+    return load().moe_route_workspace_size(ctypes.byref(cfg))
+
+
 def permute_workspace_size(cfg: MoeConfig) -> int:
     return load().moe_permute_workspace_size(ctypes.byref(cfg))
 
@@ -145,10 +151,12 @@ def route(cfg, x, W_g, W_noise=None, eps=None, bias=None, *, want_logits=False, 
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     w = torch.empty(T, k, dtype=torch.float32, device=dev)
     logits = torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None
+    ws = _workspace(route_workspace_size(cfg), dev)
     st = lib.moe_route(ctypes.byref(cfg), _ptr(x, act_dtype(cfg), "x"), _ptr(W_g, torch.float32, "W_g"),
                        _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
                        _ptr(bias, torch.float32, "bias", True), ids.data_ptr(), w.data_ptr(),
-                       logits.data_ptr() if logits is not None else None, _stream(stream))
+                       logits.data_ptr() if logits is not None else None, ws.data_ptr(), ws.numel(),
+                       _stream(stream))
     _check(st, "moe_route")
     return (ids, w, logits) if want_logits else (ids, w)
 

@@ -18,12 +18,13 @@
 #include "gemm_simt.cuh"
 #include "gemm_tc.cuh"
 #include "router.cuh"
+#include "router_tc.cuh"
 
 using namespace moe;
 
 namespace {
 
-constexpr int kVersion = (1 << 16) | 0;
+constexpr int kVersion = (1 << 16) | 1;
 constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
@@ -52,6 +53,21 @@ moe_status check_config(const moe_config* c) {
 }
 
 size_t act_bytes(const moe_config* c) { return c->act_dtype == MOE_DT_BF16 ? 2 : 4; }
+
+int router_cols(const moe_config* c) { return c->gate == MOE_GATE_NOISY ? 2 * c->n_routed : c->n_routed; }
+
+// Width of the tensor-core router tile, or 0 when the CUDA-core router runs
+// (fp32 tokens, or more than 128 router columns).
+int router_tc_np(const moe_config* c) {
+  const int cols = router_cols(c);
+  if (c->act_dtype != MOE_DT_BF16 || cols > 128) return 0;
+  return cols <= 32 ? 32 : (cols <= 64 ? 64 : 128);
+}
+
+// Bytes of the three bf16 planes of [W_g | W_noise] the tensor-core router reads.
+size_t router_planes_bytes(const moe_config* c) {
+  return static_cast<size_t>(3) * router_tc_np(c) * c->d * 2;
+}
 
 // ---------------------------------------------------------------------------
 // workspace layouts (every region 256-byte aligned)
@@ -104,7 +120,7 @@ FfnWs ffn_layout(const moe_config* c) {
 
 struct FwdWs {
   size_t ids, w, counts, offsets, dest, perm_src, blk, rank, mt_start, gsize, a_row, o_row, x_perm,
-      H, y_acc, total;
+      H, y_acc, planes, total;
 };
 FwdWs forward_layout(const moe_config* c) {
   Carver k;
@@ -126,6 +142,7 @@ FwdWs forward_layout(const moe_config* c) {
   w.x_perm = k.take(act_bytes(c) * n * c->d);
   w.H = k.take(act_bytes(c) * padded_rows(c) * c->d_ff);
   w.y_acc = c->act_dtype == MOE_DT_BF16 ? k.take(sizeof(float) * c->T * c->d) : 0;
+  w.planes = k.take(router_planes_bytes(c));
   w.total = k.off;
   return w;
 }
@@ -177,6 +194,11 @@ moe_status device_state(DeviceState** out) {
     ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiScatterAdd>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(tc_smem_bytes(kEpiScatterAdd))) == cudaSuccess;
+#define MOE_RTC_ATTR(NP)                                                                         \
+  ok &= cudaFuncSetAttribute(router_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                             static_cast<int>(RtcShape<NP>::smem_bytes)) == cudaSuccess;
+    MOE_RTC_ATTR(32) MOE_RTC_ATTR(64) MOE_RTC_ATTR(128)
+#undef MOE_RTC_ATTR
 #define MOE_ROUTER_ATTR(TX, EP)                                                                  \
   ok &= cudaFuncSetAttribute(router_kernel<TX, EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              static_cast<int>(router_smem_bytes<EP>())) == cudaSuccess;
@@ -218,7 +240,7 @@ moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : M
 // ---------------------------------------------------------------------------
 moe_status launch_route(const moe_config* c, const void* x, const float* W_g, const float* W_noise,
                         const float* eps, const float* bias, int32_t* ids, float* w, float* logits,
-                        float* zero_rows, int sm_count, cudaStream_t st) {
+                        float* zero_rows, int sm_count, void* planes, cudaStream_t st) {
   RouterArgs a;
   a.x = x;
   a.W_g = W_g;
@@ -238,6 +260,28 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   a.zero_width = c->d;
   a.w_vec4 = (c->n_routed % 4 == 0) && aligned16(W_g) && (W_noise == nullptr || aligned16(W_noise));
   const int cols = a.noisy ? 2 * a.E : a.E;
+  const int np = router_tc_np(c);
+  if (np > 0) {
+    if (c->T == 0) return MOE_OK;
+    // split [W_g | W_noise] into three bf16 planes, then the tensor-core router
+    auto* pl = static_cast<__nv_bfloat16*>(planes);
+    router_split_kernel<<<dim3(static_cast<unsigned>((c->d + 31) / 32), static_cast<unsigned>(np / 32)), 256, 0,
+                          st>>>(W_g, W_noise, c->d, c->n_routed, cols, np, pl);
+    MOE_TRY(last_launch());
+    CUtensorMap xm, wm;
+    MOE_TRY(make_map(&xm, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->d, c->T, 64, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(make_map(&wm, pl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->d, 3ull * np, 64, np,
+                     CU_TENSOR_MAP_SWIZZLE_128B));
+    const unsigned grid = static_cast<unsigned>((c->T + 127) / 128);
+    if (np == 32)
+      router_tc_kernel<32><<<grid, kRtcThreads, RtcShape<32>::smem_bytes, st>>>(xm, wm, a);
+    else if (np == 64)
+      router_tc_kernel<64><<<grid, kRtcThreads, RtcShape<64>::smem_bytes, st>>>(xm, wm, a);
+    else
+      router_tc_kernel<128><<<grid, kRtcThreads, RtcShape<128>::smem_bytes, st>>>(xm, wm, a);
+    return last_launch();
+  }
   const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
   if (nblk == 0) return MOE_OK;
   // Few token blocks (decode-sized T): a cluster of CS CTAs also splits the
@@ -451,20 +495,27 @@ const char* moe_status_string(int status) {
 
 int moe_version(void) { return kVersion; }
 
+size_t moe_route_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return router_planes_bytes(cfg);
+}
+
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
                      const float* eps, const float* bias, int32_t* topk_ids, float* topk_w,
-                     float* logits, void* stream) {
+                     float* logits, void* workspace, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
   const bool noisy = cfg->gate == MOE_GATE_NOISY;
   if (cfg->T > 0 && (x == nullptr || W_g == nullptr || topk_ids == nullptr || topk_w == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (noisy && cfg->T > 0 && (W_noise == nullptr || eps == nullptr)) return MOE_ERR_INVALID_ARG;
   if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const size_t need = router_planes_bytes(cfg);
+  if (ws_bytes < need || (need > 0 && workspace == nullptr)) return MOE_ERR_WORKSPACE;
   DeviceState* ds;
   MOE_TRY(device_state(&ds));
   return launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, topk_ids,
-                      topk_w, logits, nullptr, ds->sm_count, static_cast<cudaStream_t>(stream));
+                      topk_w, logits, nullptr, ds->sm_count, workspace, static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_permute_workspace_size(const moe_config* cfg) {
@@ -602,7 +653,7 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   MOE_TRY(mark(0));
   // 1. gate (also clears the fp32 accumulator rows of its tokens)
   MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w,
-                       nullptr, acc, ds->sm_count, st));
+                       nullptr, acc, ds->sm_count, at<void>(workspace, L.planes), st));
   MOE_TRY(mark(1));
   // 2. dispatch + group plan
   PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),

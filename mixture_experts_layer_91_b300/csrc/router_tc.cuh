@@ -1,0 +1,363 @@
+// router_tc.cuh -- the gate on the 5th-generation tensor cores (bf16 tokens).
+//
+// Same computation as router_kernel (DeepSeekMoE translation on
+// gitcode.csdn.net, section 3.2, eqs (10)-(11); noisy gate of the "Mixture of
+// Experts" notes on blog.carolineworld.cn, section 2), with the router GEMM
+// logits = x . W done on tcgen05 at fp32 accuracy:
+//
+//   * x is bf16, so every x_k is exact in bf16;
+//   * W (fp32) is split once per call into three bf16 planes,
+//       W = hi + mid + lo,  hi = rn(W), mid = rn(W - hi), lo = rn(W - hi - mid),
+//     each difference exact in fp32, so the planes carry all 24 significand
+//     bits of W (8 each);
+//   * each product x_k * plane_k is exact in fp32 (8 x 8 significand bits);
+//   * the tensor core sums only short runs: every kRtcChunk k-blocks (128
+//     k-elements) the partial sums are drained from tensor memory and added
+//     into fp32 registers with ordinary round-to-nearest adds. The tensor
+//     core's own accumulation is not an IEEE add chain: over a whole row of
+//     d = 4096 its rounding reached ~1e-5 on logits of size ~4, the size of
+//     the routing margin; over 128 elements it stays far below.
+// So the logits are an fp32 dot product of the exact inputs, as the fp32
+// router asks ("Mixture of Experts" notes, section 5, ST-MoE precision).
+//
+// One CTA owns a 128-token tile; 6 warps:
+//   warp 0      TMA producer: x [128 x 64] and the three W planes [NP x 64]
+//               per k-block into a multi-stage ring;
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma
+//               M=128 K=16 with the three planes stacked as one B operand
+//               (N = 3 NP; at NP = 128 one N = 256 MMA for hi | mid and one
+//               N = 128 MMA adding lo onto mid, whose products are 2^-9
+//               smaller, so sharing their accumulator costs nothing),
+//               double-buffered over chunks;
+//   warps 2-5   clear the tile's rows of the fp32 combine accumulator (forward
+//               path), then drain each chunk (warp w reads the TMEM lanes of
+//               quarter w % 4: one token per thread) into NP fp32 registers,
+//               and finally compute that token's softmax and top-k in
+//               registers (eight interleaved arg-max chains per round, ties to
+//               the lower expert index).
+#pragma once
+
+#include "common.cuh"
+#include "router.cuh"
+
+namespace moe {
+
+constexpr int kRtcThreads = 192;
+constexpr int kRtcChunk = 2;   // k-blocks (of 64) per tensor-memory drain
+
+template <int NP>
+struct RtcShape {
+  static_assert(NP == 32 || NP == 64 || NP == 128, "router tile width");
+  static constexpr int STAGES = NP <= 64 ? 4 : 3;
+  static constexpr uint32_t A_BYTES = 128 * 64 * 2;   // x tile, 128 tokens x 64 k
+  static constexpr uint32_t B_BYTES = NP * 64 * 2;    // one W plane, NP columns x 64 k
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + 3 * B_BYTES;
+  static constexpr int LS = NP + 1;                   // row stride of the per-token logits rows
+  // One accumulator buffer holds hi | mid | lo side by side (3 NP columns)
+  // when 3 NP <= 256, so one MMA of N = 3 NP covers all three planes; at
+  // NP = 128 it holds hi | (mid + lo) (256 columns): one MMA of N = 256 for
+  // hi | mid and one of N = 128 adding lo onto the mid columns.
+  static constexpr bool STACK3 = 3 * NP <= 256;
+  static constexpr uint32_t BUF_COLS = NP == 32 ? 128 : 256;   // column stride of the 2 buffers
+  static constexpr uint32_t TMEM_COLS = 2 * BUF_COLS;
+  static constexpr size_t smem_bytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 128;
+  static_assert(128ull * LS * 4 <= static_cast<size_t>(STAGES) * STAGE_BYTES, "epilogue rows");
+};
+
+// The three bf16 planes of W = [W_g | W_noise] ([d, cols] fp32, row-major),
+// stored K-major: planes[p][n][k], n < NP (rows n >= cols are zero).
+__global__ void __launch_bounds__(256)
+    router_split_kernel(const float* __restrict__ W_g, const float* __restrict__ W_noise, int32_t d,
+                        int32_t E, int32_t cols, int32_t NP, __nv_bfloat16* __restrict__ planes) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+  for (int r = ty; r < 32; r += 8) {
+    const int k = k0 + r, n = n0 + tx;
+    float v = 0.f;
+    if (k < d && n < cols)
+      v = n < E ? W_g[static_cast<int64_t>(k) * E + n] : W_noise[static_cast<int64_t>(k) * E + (n - E)];
+    tile[r][tx] = v;
+  }
+  __syncthreads();
+  const size_t plane = static_cast<size_t>(NP) * d;
+  for (int r = ty; r < 32; r += 8) {
+    const int n = n0 + r, k = k0 + tx;
+    if (n < NP && k < d) {
+      const float w = tile[tx][r];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+      const float r1 = w - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(mid);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+      const size_t o = static_cast<size_t>(n) * d + k;
+      planes[o] = hi;
+      planes[plane + o] = mid;
+      planes[2 * plane + o] = lo;
+    }
+  }
+}
+
+// (key, index) arg-max step for a scan in increasing index: a strictly larger
+// key wins, so equal keys keep the lower index; NaN marks an entry that is
+// out of range or already taken and never wins.
+__device__ __forceinline__ void argmax_step(float kc, int c, float& kb, int& ib) {
+  if (kc > kb || (kb != kb && kc == kc)) {
+    kb = kc;
+    ib = c;
+  }
+}
+
+// Merge two candidates from scans over different index sets.
+__device__ __forceinline__ void argmax_merge(float ko, int io, float& kb, int& ib) {
+  const bool take = (ko == ko) && ((kb != kb) || ko > kb || (ko == kb && io < ib));
+  if (take) {
+    kb = ko;
+    ib = io;
+  }
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kRtcThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                     const RouterArgs p) {
+  using S = RtcShape<NP>;
+  extern __shared__ uint8_t rtc_smem_raw[];
+  const uint32_t raw = smem_addr(rtc_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = rtc_smem_raw + (base - raw);
+  const uint32_t sBar = base + S::STAGES * S::STAGE_BYTES;
+  uint8_t* gBar = gbase + S::STAGES * S::STAGE_BYTES;
+  const uint32_t bar_full = sBar;                    // [STAGES]
+  const uint32_t bar_empty = sBar + 8 * S::STAGES;   // [STAGES]
+  const uint32_t bar_tfull = sBar + 16 * S::STAGES;  // [2]
+  const uint32_t bar_tempty = bar_tfull + 16;        // [2]
+  const uint32_t bar_done = bar_tempty + 16;         // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 16 * S::STAGES + 40);
+  volatile int* abort = reinterpret_cast<volatile int*>(gBar + 16 * S::STAGES + 44);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 4);
+    }
+    mbar_init(bar_done, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&wmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int32_t nk = (p.d + 63) / 64;
+  const int32_t nchunk = (nk + kRtcChunk - 1) / kRtcChunk;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int32_t kb = 0;
+      bool ok = true;
+      for (; kb < nk; ++kb) {
+        const uint32_t s = kb % S::STAGES;
+        const uint32_t ph = (kb / S::STAGES) & 1u;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort)) { ok = false; break; }
+        const uint32_t full = bar_full + 8 * s;
+        mbar_arrive_expect_tx(full, S::STAGE_BYTES);
+        const uint32_t sa = base + s * S::STAGE_BYTES;
+        tma_load_2d(sa, &xmap, full, kb * 64, static_cast<int32_t>(t0));
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl)
+          tma_load_2d(sa + S::A_BYTES + pl * S::B_BYTES, &wmap, full, kb * 64, pl * NP);
+      }
+      if (!ok) {   // the loads already issued must land before the CTA exits
+        for (int32_t j = kb > S::STAGES ? kb - S::STAGES : 0; j < kb; ++j) {
+          volatile int never = 0;
+          mbar_wait(bar_full + 8 * (j % S::STAGES), (j / S::STAGES) & 1u, &never, 100000000ull);
+        }
+      }
+    }
+    return;
+  }
+  if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NP);
+      bool ok = true;
+      int32_t kb = 0;
+      for (int32_t ch = 0; ch < nchunk && ok; ++ch) {
+        const uint32_t b = ch & 1;
+        if (!mbar_wait(bar_tempty + 8 * b, ((ch >> 1) & 1u) ^ 1u, abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem_base + b * S::BUF_COLS;
+        for (int32_t j = 0; j < kRtcChunk && kb < nk; ++j, ++kb) {
+          const uint32_t s = kb % S::STAGES;
+          const uint32_t ph = (kb / S::STAGES) & 1u;
+          if (!mbar_wait(bar_full + 8 * s, ph, abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + s * S::STAGE_BYTES;
+          const uint64_t ad = sdesc_kmajor_sw128(sa);
+          const uint64_t bd = sdesc_kmajor_sw128(sa + S::A_BYTES);   // hi, mid, lo rows stacked
+          if constexpr (S::STACK3) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 3 * NP);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc, (j | kk) != 0);
+          } else {
+            constexpr uint32_t idesc2 = idesc_bf16_f32(128, 2 * NP);
+            constexpr uint32_t idesc1 = idesc_bf16_f32(128, NP);
+            const uint64_t bl = sdesc_kmajor_sw128(sa + S::A_BYTES + 2 * S::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc2, (j | kk) != 0);
+              tc_mma_bf16(acc + NP, ad + 2 * kk, bl + 2 * kk, idesc1, 1);
+            }
+          }
+          tc_commit(bar_empty + 8 * s);
+        }
+        tc_commit(bar_tfull + 8 * b);
+      }
+      // every MMA issued must be complete before tensor memory is released
+      tc_commit(bar_done);
+      volatile int never = 0;
+      mbar_wait(bar_done, 0, &never, 100000000ull);
+    }
+    __syncwarp();
+    // the drain warps are done with tensor memory once all 160 threads meet here
+    asm volatile("bar.sync 1, 160;" ::: "memory");
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+    return;
+  }
+
+  // ---------------------------------------------------------------- warps 2-5
+  const int q = warp & 3;                       // TMEM lane quarter = token group
+  const int row = q * 32 + lane;                // token of this thread within the tile
+  if (p.zero_rows != nullptr) {
+    const int64_t rows = (p.T - t0 < 128) ? (p.T - t0) : 128;
+    float4* z = reinterpret_cast<float4*>(p.zero_rows + t0 * p.zero_width);
+    const int64_t n4 = rows * p.zero_width / 4;
+    for (int64_t i = threadIdx.x - 64; i < n4; i += 128) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float acc[NP];
+#pragma unroll
+  for (int c = 0; c < NP; ++c) acc[c] = 0.f;
+  bool ok = true;
+  const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  for (int32_t ch = 0; ch < nchunk; ++ch) {
+    const uint32_t b = ch & 1;
+    ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_tfull + 8 * b, (ch >> 1) & 1u, abort));
+    if (!ok) break;
+    tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < NP / 32; ++cc) {
+      const uint32_t col = tl + b * S::BUF_COLS + cc * 32;
+      uint32_t hi[32], mid[32];
+      tmem_ld_32x32b_x32(col, hi);
+      tmem_ld_32x32b_x32(col + NP, mid);
+      if constexpr (S::STACK3) {
+        uint32_t lo[32];
+        tmem_ld_32x32b_x32(col + 2 * NP, lo);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          acc[cc * 32 + j] += __uint_as_float(hi[j]) + (__uint_as_float(mid[j]) + __uint_as_float(lo[j]));
+      } else {
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(mid[j]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
+  }
+  // tensor memory is no longer read: let warp 1 free it
+  tc_fence_before();
+  asm volatile("bar.arrive 1, 160;" ::: "memory");
+
+  const int64_t t = t0 + row;
+  if (!ok || t >= p.T) return;
+  const int E = p.E;
+
+  // logits row in shared memory (the operand ring is idle now: every load
+  // landed and every MMA that read it completed) for the lookups of the picks
+  float* Lrow = reinterpret_cast<float*>(gbase) + row * S::LS;
+#pragma unroll
+  for (int c = 0; c < NP; ++c) Lrow[c] = acc[c];
+  if (p.logits_out != nullptr)
+    for (int c = 0; c < E; ++c) p.logits_out[t * E + c] = Lrow[c];
+
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < NP; ++c)
+    if (c < E) mx[c & 3] = fmaxf(mx[c & 3], acc[c]);
+  const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < NP; ++c)
+    if (c < E) sm[c & 3] += expf(acc[c] - m);
+  const float inv = 1.0f / ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+
+  // selection keys, in place; NaN = not selectable
+  const float nan = __int_as_float(0x7fffffff);
+#pragma unroll
+  for (int c = 0; c < NP; ++c) {
+    float key = nan;
+    if (c < E) {
+      if (p.noisy) key = acc[c] + p.eps[t * E + c] * softplus_f(Lrow[c + E]);
+      else if (p.bias != nullptr) key = expf(acc[c] - m) * inv + __ldg(p.bias + c);
+      else key = acc[c];   // Softmax is increasing: the order of s is the order of the logits
+      if (key != key) key = -INFINITY;   // a NaN key ranks last, ids stay valid
+    }
+    acc[c] = key;
+  }
+
+  float sel_sum = 0.f, key0 = 0.f;
+  for (int r = 0; r < p.k; ++r) {
+    float kb8[8];
+    int ib8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      kb8[j] = nan;
+      ib8[j] = -1;
+    }
+#pragma unroll
+    for (int c = 0; c < NP; ++c) argmax_step(acc[c], c, kb8[c & 7], ib8[c & 7]);
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) argmax_merge(kb8[j + w], ib8[j + w], kb8[j], ib8[j]);
+    const float kb = kb8[0];
+    const int bi = ib8[0];   // k <= E: a selectable entry remains every round
+#pragma unroll
+    for (int c = 0; c < NP; ++c) acc[c] = (c == bi) ? nan : acc[c];
+    float v;
+    if (p.noisy) {
+      if (r == 0) key0 = kb;
+      v = expf(kb - key0);             // softmax over the kept H (max is the first pick)
+    } else {
+      v = expf(Lrow[bi] - m) * inv;    // s of the pick
+    }
+    sel_sum += v;
+    p.topk_ids[t * p.k + r] = bi;
+    p.topk_w[t * p.k + r] = v;
+  }
+  if (p.noisy || p.renorm)
+    for (int r = 0; r < p.k; ++r) p.topk_w[t * p.k + r] /= sel_sum;
+}
+
+}  // namespace moe

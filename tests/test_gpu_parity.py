@@ -25,8 +25,12 @@ pytestmark = pytest.mark.gpu
 MARGIN = 1e-5
 DEV = "cuda"
 
+# bf16 tokens with more than 128 router columns take the CUDA-core router
+WIDE_ROUTER = workloads.Workload("wide_router_bf16_T777", T=777, d=512, n_routed=160, n_shared=1,
+                                 top_k=8, d_ff=128, seed=17)
 SMALL = [
     workloads.TINY_FP32,
+    WIDE_ROUTER,
     workloads.DSMOE_2B.with_tokens(700),
     workloads.DSMOE_16B.with_tokens(333),
     workloads.GSHARD_NOISY.with_tokens(300),

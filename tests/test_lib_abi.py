@@ -74,14 +74,14 @@ def test_invalid_configs_rejected(lib, bad):
                                  dict(gate=1, renormalize=1, n_routed=129), dict(top_k=33, n_routed=64)])
 def test_unsupported_configs(lib, bad):
     c = cfg_of(**bad)
-    st = lib.moe_route(ctypes.byref(c), *([None] * 8), None)
+    st = lib.moe_route(ctypes.byref(c), *([None] * 8), None, 0, None)
     assert st == 2   # MOE_ERR_UNSUPPORTED
 
 
 def test_null_pointers_and_workspace_checked_before_launch(lib):
     c = cfg_of()
     assert fwd_nulls(lib, None) == 1
-    assert lib.moe_route(ctypes.byref(c), *([None] * 8), None) == 1
+    assert lib.moe_route(ctypes.byref(c), *([None] * 8), None, 0, None) == 1
     # a too-small workspace is reported before anything touches the device
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
     st = lib.moe_forward(ctypes.byref(c), fake, fake, None, None, None, fake, fake, fake, fake, 16,
