@@ -315,7 +315,10 @@ def main():
     tflops = world * flops / (ms_step / 1e3) / 1e12
     ab = algorithmic_bytes(w, touched)
     roof_time = max(flops / (pk["bf16_tflops"] * 1e12), ab / (pk["hbm_gbs"] * 1e9))
-    launches_per_step = 7 if not w.fp32 else 6
+    # bf16: [W split] + router + count + scan + rank + gate-up + down + cast;
+    # fp32: router + count + scan + scatter + gate-up + down
+    tc_router = (not w.fp32) and (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
+    launches_per_step = 6 if w.fp32 else (8 if tc_router else 7)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

@@ -83,8 +83,8 @@ const char* moe_status_string(int status);
 int moe_version(void);
 
 /* Bytes of scratch moe_route needs: the three bf16 planes of the router
- * weights read by the tensor-core router (0 for fp32 tokens or more than 128
- * router columns, where the CUDA-core router runs). */
+ * weights read by the tensor-core router (0 where the CUDA-core router runs:
+ * fp32 tokens, more than 128 router columns, or T < 4096). */
 size_t moe_route_workspace_size(const moe_config* cfg);
 
 /*
@@ -105,10 +105,10 @@ size_t moe_route_workspace_size(const moe_config* cfg);
  *   workspace, ws_bytes              scratch, >= moe_route_workspace_size()
  *                                    (may be NULL when that is 0)
  * The logits are an fp32-accurate dot product of the stored inputs. bf16
- * tokens with at most 128 router columns (N_r, or 2 N_r when noisy) run on
- * the tensor cores: W is split exactly into three bf16 planes, every
- * product is exact, and the accumulation is fp32. Otherwise a CUDA-core fp32
- * FMA kernel runs. Softmax, keys and gates are fp32.
+ * tokens with at most 128 router columns (N_r, or 2 N_r when noisy) and
+ * T >= 4096 run on the tensor cores: W is split exactly into three bf16
+ * planes, every product is exact, and the accumulation is fp32. Otherwise a
+ * CUDA-core fp32 FMA kernel runs. Softmax, keys and gates are fp32.
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g,
                      const float* W_noise, const float* eps, const float* bias,

@@ -18,7 +18,9 @@
 //   warp 1      allocates 512 TMEM columns; one thread issues
 //               tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of two
 //               TMEM accumulators and commits stage / accumulator barriers.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns one
+//   warps 2..5  epilogue: (gate-up, forward path: first clear a share of the
+//               fp32 combine accumulator while the first MMAs run) then
+//               tcgen05.ld of the accumulator (each warp owns one
 //               32-lane quarter), then
 //                 gate-up : h = silu(acc[:, 0:128]) * acc[:, 128:256] -> bf16,
 //                           staged in shared memory, TMA-stored to H;
@@ -75,6 +77,8 @@ struct TcArgs {
   const float* topk_w;      // down scatter: gate values [T*k]
   int32_t top_k;
   int32_t fold_mt;          // down scatter with K_s > 0: m-tiles per shared group, else 0
+  float4* zero_out;         // gate-up: buffer the epilogue warps clear (fp32 combine accumulator)
+  int64_t zero_n4;          // its size in float4
 };
 
 struct TcMaps {
@@ -277,6 +281,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ew = warp - 2;        // epilogue warp 0..3
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     uint32_t local = 0, nstore = 0;
+    if (MODE == kEpiSwiGLU && p.zero_out != nullptr) {
+      // clear this CTA's share of the combine accumulator while the first MMAs run
+      const int64_t per = (p.zero_n4 + gridDim.x - 1) / gridDim.x;
+      const int64_t z0 = static_cast<int64_t>(blockIdx.x) * per;
+      const int64_t z1 = z0 + per < p.zero_n4 ? z0 + per : p.zero_n4;
+      for (int64_t i = z0 + (threadIdx.x - 64); i < z1; i += kTcEpiWarps * 32)
+        p.zero_out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     for (int32_t t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       const TileCoord c = decode_tile(t, p.n_tiles, p.plan.mt_start, p.G, p.n_shared, p.fold_mt, nk);
       const uint32_t b = local & 1u;

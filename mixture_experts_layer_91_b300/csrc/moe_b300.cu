@@ -54,13 +54,17 @@ moe_status check_config(const moe_config* c) {
 
 size_t act_bytes(const moe_config* c) { return c->act_dtype == MOE_DT_BF16 ? 2 : 4; }
 
+constexpr int64_t kRouterTcMinTokens = 4096;
+
 int router_cols(const moe_config* c) { return c->gate == MOE_GATE_NOISY ? 2 * c->n_routed : c->n_routed; }
 
 // Width of the tensor-core router tile, or 0 when the CUDA-core router runs
 // (fp32 tokens, or more than 128 router columns).
 int router_tc_np(const moe_config* c) {
   const int cols = router_cols(c);
-  if (c->act_dtype != MOE_DT_BF16 || cols > 128) return 0;
+  // the tensor-core router spreads its work over one CTA per 128 tokens; below
+  // 32 such tiles the CUDA-core router (cluster split-K) keeps more SMs busy
+  if (c->act_dtype != MOE_DT_BF16 || cols > 128 || c->T < kRouterTcMinTokens) return 0;
   return cols <= 32 ? 32 : (cols <= 64 ? 64 : 128);
 }
 
@@ -351,11 +355,14 @@ moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void
 }
 
 // Gate-up (SwiGLU fused) into H, then the down projection with epilogue `mode`.
+// The gate-up GEMM also clears `zero` (the bf16 forward path's fp32 combine
+// accumulator, zero_n4 float4s) on the side.
 moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void* x,
                           const void* x_perm, const GroupPlan& plan, const void* W1, const void* W3,
                           const void* W2, void* H, int mode, float* out, const int32_t* perm_src,
                           const float* topk_w, cudaStream_t st,
-                          const std::function<moe_status(int)>* mark = nullptr) {
+                          const std::function<moe_status(int)>* mark = nullptr,
+                          float* zero = nullptr, int64_t zero_n4 = 0) {
   const int G = n_groups(c);
   const int64_t P = padded_rows(c);
   const int I = c->d_ff, d = c->d;
@@ -389,6 +396,8 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.n_tiles = (I + kTcBN / 2 - 1) / (kTcBN / 2);
     a.b_rows = I;
     a.n_out = I;
+    a.zero_out = reinterpret_cast<float4*>(zero);
+    a.zero_n4 = zero != nullptr ? zero_n4 : 0;
     grouped_gemm_tc<kEpiSwiGLU><<<grid, kTcThreads, tc_smem_bytes(kEpiSwiGLU), st>>>(gu, a);
     MOE_TRY(last_launch());
     if (mark) MOE_TRY((*mark)(3));
@@ -398,6 +407,8 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.b_rows = d;
     a.n_out = d;
     a.out = out;
+    a.zero_out = nullptr;
+    a.zero_n4 = 0;
     // the combine folds the shared experts into one group (gate 1 for all)
     a.fold_mt = (mode == kEpiScatterAdd && c->n_shared > 0) ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
     if (mode == kEpiScatterAdd)
@@ -651,9 +662,11 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
     return MOE_ERR_CUDA;
   };
   MOE_TRY(mark(0));
-  // 1. gate (also clears the fp32 accumulator rows of its tokens)
+  // 1. gate
+  // (the fp32 router also clears y, the fp32 combine target; for bf16 the
+  // gate-up GEMM clears the accumulator)
   MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w,
-                       nullptr, acc, ds->sm_count, at<void>(workspace, L.planes), st));
+                       nullptr, bf ? nullptr : acc, ds->sm_count, at<void>(workspace, L.planes), st));
   MOE_TRY(mark(1));
   // 2. dispatch + group plan
   PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
@@ -667,7 +680,8 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   // 3. experts: gate-up + SwiGLU, then down with the gate-weighted scatter-add
   GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
   MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H),
-                         kEpiScatterAdd, acc, perm_src, w, st, stage_events ? &mark : nullptr));
+                         kEpiScatterAdd, acc, perm_src, w, st, stage_events ? &mark : nullptr,
+                         bf ? acc : nullptr, cfg->T * cfg->d / 4));
   // 4. fp32 accumulator -> bf16 output
   if (bf) {
     const int64_t n8 = cfg->T * cfg->d / 8;
