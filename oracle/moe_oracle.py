@@ -176,7 +176,35 @@ def dense_gates(ids: np.ndarray, gates: np.ndarray, n_experts: int) -> np.ndarra
 # Dispatch: per-expert counts and token groups
 # --------------------------------------------------------------------------
 
-def dispatch(ids: np.ndarray, n_experts: int) -> dict:
+def capacity_keep(ids: np.ndarray, n_experts: int, capacity: int) -> np.ndarray:
+    """Which assignments an expert with a capacity accepts.
+
+    [MoE-notes] section 3 (GShard, expert capacity): the gate keeps a running
+    counter c_e of the tokens sent to expert e; once c_e reaches the capacity
+    the expert takes no more, and the overflowing token's assignment is
+    dropped (its gate for that expert becomes zero; the token still reaches
+    the output through the residual). Section 4 (Switch) sets the capacity to
+    tokens/experts x capacity factor. Reading: tokens arrive in ascending
+    order, and a token's k picks in its listed order, i.e. ascending flat
+    assignment index t*k + j. capacity = 0 means no limit (the DeepSeekMoE
+    layer is dropless). Returns keep [T, k] bool.
+    """
+    ids = np.asarray(ids)
+    keep = np.ones(ids.shape, dtype=bool)
+    if capacity <= 0:
+        return keep
+    c = np.zeros(n_experts, dtype=np.int64)   # the running counters c_e
+    for t in range(ids.shape[0]):
+        for j in range(ids.shape[1]):
+            e = int(ids[t, j])
+            if c[e] < capacity:
+                c[e] += 1
+            else:
+                keep[t, j] = False
+    return keep
+
+
+def dispatch(ids: np.ndarray, n_experts: int, capacity: int = 0) -> dict:
     """Group the T*k assignments by expert.
 
     The pages state only that each token is assigned to its selected experts
@@ -187,16 +215,23 @@ def dispatch(ids: np.ndarray, n_experts: int) -> dict:
     of counts), in ascending flat assignment index t*k + j (so ascending
     token within an expert).
 
-    Returns counts [E], offsets [E+1], perm_src [T*k] (flat assignment index
-    of each grouped row) and dest [T, k] (grouped row of each assignment).
+    With a capacity (capacity_keep), dropped assignments take no row: counts
+    are the accepted counts, and their dest is -1.
+
+    Returns counts [E], offsets [E+1], perm_src [sum(counts)] (flat assignment
+    index of each grouped row) and dest [T, k] (grouped row of each
+    assignment, -1 if dropped).
     """
-    flat = np.asarray(ids).reshape(-1)
-    counts = np.bincount(flat, minlength=n_experts).astype(np.int64)
+    ids = np.asarray(ids)
+    flat = ids.reshape(-1)
+    kept = capacity_keep(ids, n_experts, capacity).reshape(-1)
+    counts = np.bincount(flat[kept], minlength=n_experts).astype(np.int64)
     offsets = np.zeros(n_experts + 1, dtype=np.int64)
     offsets[1:] = np.cumsum(counts)
-    perm_src = np.argsort(flat, kind="stable")
-    dest = np.empty_like(perm_src)
-    dest[perm_src] = np.arange(flat.size)
+    order = np.argsort(flat, kind="stable")
+    perm_src = order[kept[order]]
+    dest = np.full(flat.size, -1, dtype=np.int64)
+    dest[perm_src] = np.arange(perm_src.size)
     return {"counts": counts, "offsets": offsets, "perm_src": perm_src,
             "dest": dest.reshape(ids.shape)}
 
@@ -225,8 +260,16 @@ def expert_ffn_relu(X, wi, wo) -> np.ndarray:
     return h @ _f64(wo).T
 
 
+def ffn(X, W1, W3, W2, act: str = "swiglu") -> np.ndarray:
+    """The expert FFN of the layer: SwiGLU W2 (silu(W1 x) * (W3 x)), or GShard's
+    W2 . ReLU(W1 x) (act = "relu", W3 unused)."""
+    if act == "relu":
+        return expert_ffn_relu(X, W1, W2)
+    return expert_ffn(X, W1, W3, W2)
+
+
 def moe_forward(x, W1, W3, W2, n_shared: int, ids, gates,
-                tokens=None) -> np.ndarray:
+                tokens=None, act: str = "swiglu", keep=None) -> np.ndarray:
     """Layer output without the residual:
         y_t = sum_{i<K_s} FFN_i(u_t) + sum_{j<k} g_{t,j} FFN_{K_s+ids[t,j]}(u_t).
 
@@ -236,27 +279,33 @@ def moe_forward(x, W1, W3, W2, n_shared: int, ids, gates,
     where G(x)_i = 0): each expert runs only on the tokens that select it.
 
     `tokens` (optional) restricts the output to a subset of token indices;
-    tokens are independent, so the rows of that subset are exact.
+    tokens are independent, so the rows of that subset are exact. `act`
+    selects the expert FFN (see ffn). `keep` [T, k] (optional, from
+    capacity_keep) drops the assignments an expert's capacity refused.
     Returns y [len(tokens) or T, d] fp64.
     """
     x = _f64(x)
     ids = np.asarray(ids)
     gates = _f64(gates)
+    if keep is not None:
+        gates = np.where(np.asarray(keep), gates, 0.0)
+        ids = np.where(np.asarray(keep), ids, -1)
     if tokens is None:
         tokens = np.arange(x.shape[0])
     tokens = np.asarray(tokens)
     xs = x[tokens]
     ids_s = ids[tokens]
     g_s = gates[tokens]
+    W3i = (lambda i: None) if act == "relu" else (lambda i: W3[i])
     y = np.zeros((tokens.size, x.shape[1]), dtype=F64)
     for i in range(n_shared):
-        y += expert_ffn(xs, W1[i], W3[i], W2[i])
+        y += ffn(xs, W1[i], W3i(i), W2[i], act)
     n_routed = W1.shape[0] - n_shared
     for e in range(n_routed):
         rows, slot = np.nonzero(ids_s == e)
         if rows.size == 0:
             continue
-        o = expert_ffn(xs[rows], W1[n_shared + e], W3[n_shared + e], W2[n_shared + e])
+        o = ffn(xs[rows], W1[n_shared + e], W3i(n_shared + e), W2[n_shared + e], act)
         np.add.at(y, rows, g_s[rows, slot][:, None] * o)
     return y
 
@@ -276,7 +325,8 @@ def moe_forward_dense(x, W1, W3, W2, n_shared: int, G) -> np.ndarray:
     return y
 
 
-def expert_rows(x, W1, W3, W2, n_shared: int, perm_src, offsets, top_k: int) -> np.ndarray:
+def expert_rows(x, W1, W3, W2, n_shared: int, perm_src, offsets, top_k: int,
+                act: str = "swiglu") -> np.ndarray:
     """Per-row expert outputs, unweighted, in the grouped layout.
 
     Rows [0, K_s*T): shared expert i on token t at row i*T + t.
@@ -285,16 +335,17 @@ def expert_rows(x, W1, W3, W2, n_shared: int, perm_src, offsets, top_k: int) -> 
     """
     x = _f64(x)
     T = x.shape[0]
+    W3i = (lambda i: None) if act == "relu" else (lambda i: W3[i])
     out = np.zeros((n_shared * T + perm_src.size, x.shape[1]), dtype=F64)
     for i in range(n_shared):
-        out[i * T:(i + 1) * T] = expert_ffn(x, W1[i], W3[i], W2[i])
+        out[i * T:(i + 1) * T] = ffn(x, W1[i], W3i(i), W2[i], act)
     n_routed = offsets.size - 1
     for e in range(n_routed):
         a, b = int(offsets[e]), int(offsets[e + 1])
         if b > a:
             toks = np.asarray(perm_src[a:b]) // top_k
-            out[n_shared * T + a:n_shared * T + b] = expert_ffn(
-                x[toks], W1[n_shared + e], W3[n_shared + e], W2[n_shared + e])
+            out[n_shared * T + a:n_shared * T + b] = ffn(
+                x[toks], W1[n_shared + e], W3i(n_shared + e), W2[n_shared + e], act)
     return out
 
 
@@ -307,7 +358,10 @@ def combine(rows, dest, gates, n_shared: int, T: int) -> np.ndarray:
     y = np.zeros((T, rows.shape[1]), dtype=F64)
     for i in range(n_shared):
         y += rows[i * T:(i + 1) * T]
-    y += np.einsum("tk,tkd->td", gates, rows[n_shared * T + np.asarray(dest)])
+    dest = np.asarray(dest)
+    kept = dest >= 0   # assignments an expert's capacity dropped add nothing
+    y += np.einsum("tk,tkd->td", np.where(kept, gates, 0.0),
+                   rows[n_shared * T + np.where(kept, dest, 0)])
     return y
 
 
@@ -365,6 +419,21 @@ def switch_balance_loss(p, alpha: float) -> float:
     f = np.bincount(top1[:, 0], minlength=N) / T
     P = p.mean(axis=0)
     return float(alpha * N * np.sum(f * P))
+
+
+def logsumexp(logits) -> np.ndarray:
+    """Per-token log sum_j exp(x_j), with max subtraction: the term the router
+    z-loss squares ([MoE-notes] section 5, ST-MoE). [T]."""
+    z = _f64(logits)
+    m = z.max(axis=1, keepdims=True)
+    return m[:, 0] + np.log(np.exp(z - m).sum(axis=1))
+
+
+def prob_column_sums(logits) -> np.ndarray:
+    """sum_t s_{i,t}: the softmax router probabilities summed over tokens, so
+    that P_i = (1/T) of it ([DSMoE] section 3.3, eq (14); the Switch loss's
+    P_i, [MoE-notes] section 4). [E]."""
+    return softmax(logits).sum(axis=0)
 
 
 def router_z_loss(logits) -> float:

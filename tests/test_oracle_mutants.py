@@ -13,7 +13,8 @@ from tests import test_oracle_pins as P
 
 _orig = {name: getattr(O, name) for name in
          ("silu", "topk_order", "softmax", "expert_ffn", "moe_forward", "route",
-          "dispatch", "combine", "softplus", "cv_squared", "expert_balance_loss")}
+          "dispatch", "combine", "softplus", "cv_squared", "expert_balance_loss",
+          "capacity_keep", "expert_ffn_relu", "logsumexp")}
 
 
 def _silu_relu(z):
@@ -48,8 +49,10 @@ def _ffn_w2_transposed(X, W1, W3, W2):
     return h @ W2.reshape(W2.shape[1], W2.shape[0])     # reinterpreted, not transposed
 
 
-def _forward_no_shared(x, W1, W3, W2, n_shared, ids, gates, tokens=None):
-    y = _orig["moe_forward"](x, W1, W3, W2, n_shared, ids, gates, tokens)
+def _forward_no_shared(x, W1, W3, W2, n_shared, ids, gates, tokens=None, **kw):
+    if kw.get("act", "swiglu") != "swiglu":
+        return _orig["moe_forward"](x, W1, W3, W2, n_shared, ids, gates, tokens, **kw)
+    y = _orig["moe_forward"](x, W1, W3, W2, n_shared, ids, gates, tokens, **kw)
     xs = np.asarray(x, float) if tokens is None else np.asarray(x, float)[tokens]
     for i in range(n_shared):
         y = y - _orig["expert_ffn"](xs, W1[i], W3[i], W2[i])
@@ -69,8 +72,10 @@ def _route_bias_in_gate(x, W_g, top_k, **kw):
     return r
 
 
-def _dispatch_descending(ids, n_experts):
-    d = _orig["dispatch"](ids, n_experts)
+def _dispatch_descending(ids, n_experts, capacity=0):
+    d = _orig["dispatch"](ids, n_experts, capacity)
+    if capacity:
+        return d
     flat = np.asarray(ids).reshape(-1)
     order = np.lexsort((-np.arange(flat.size), flat))     # within expert: descending index
     dest = np.empty_like(order)
@@ -96,6 +101,22 @@ def _expbal_no_norm(ids, s, n_routed, top_k, alpha1):
     return _orig["expert_balance_loss"](ids, s, n_routed, top_k, alpha1) * top_k
 
 
+def _capacity_keeps_latest(ids, n_experts, capacity):
+    # counts from the last token backwards: keeps the latest arrivals instead
+    ids = np.asarray(ids)
+    return _orig["capacity_keep"](ids[::-1, ::-1], n_experts, capacity)[::-1, ::-1]
+
+
+def _relu_without_max(X, wi, wo):
+    return (np.asarray(X, float) @ np.asarray(wi, float).T) @ np.asarray(wo, float).T
+
+
+def _logsumexp_no_max(logits):
+    z = np.asarray(logits, float)
+    m = z.max(axis=1, keepdims=True)
+    return np.log(np.exp(z - m).sum(axis=1))      # the max term dropped
+
+
 def _run_pins():
     pins = [
         lambda: P.test_softplus_and_silu_closed_forms(),
@@ -114,6 +135,12 @@ def _run_pins():
         lambda: P.test_combine_plain_loop(),
         lambda: P.test_cv_squared_hand_values(),
         lambda: P.test_balance_losses_uniform_routing(),
+        lambda: P.test_capacity_keep_matches_counting(0, 1),
+        lambda: P.test_capacity_hot_expert_keeps_first_tokens(),
+        lambda: P.test_capacity_forward_drops_only_refused_assignments(),
+        lambda: P.test_relu_expert_closed_form(),
+        lambda: P.test_relu_layer_matches_plain_loops(),
+        lambda: P.test_logsumexp_and_probability_sums_closed_forms(),
     ]
     failed = 0
     for pin in pins:
@@ -138,6 +165,9 @@ MUTANTS = {
     "softplus_as_exp": ("softplus", _softplus_exp),
     "cv_sample_variance": ("cv_squared", _cv_sample),
     "expbal_missing_k": ("expert_balance_loss", _expbal_no_norm),
+    "capacity_keeps_latest": ("capacity_keep", _capacity_keeps_latest),
+    "relu_without_max": ("expert_ffn_relu", _relu_without_max),
+    "logsumexp_drops_max": ("logsumexp", _logsumexp_no_max),
 }
 
 

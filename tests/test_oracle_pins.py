@@ -321,7 +321,109 @@ def test_combine_plain_loop():
         np.testing.assert_allclose(y[t], want, rtol=1e-14)
 
 
+# ---------------------------------------------------------------- expert capacity (GShard / Switch)
+
+def py_capacity_keep(ids, capacity):
+    """An assignment is accepted iff fewer than `capacity` earlier assignments
+    (ascending t*k + j) chose the same expert -- the running counter c_e of
+    the GShard passage, counted afresh for every assignment."""
+    T, k = len(ids), len(ids[0])
+    flat = [int(v) for row in ids for v in row]
+    keep = []
+    for a, e in enumerate(flat):
+        earlier = sum(1 for b in range(a) if flat[b] == e)
+        keep.append(earlier < capacity)
+    return np.array(keep).reshape(T, k)
+
+
+@pytest.mark.parametrize("seed,capacity", [(0, 1), (1, 3), (2, 5), (3, 9)])
+def test_capacity_keep_matches_counting(seed, capacity):
+    rng = np.random.default_rng(seed)
+    T, E, k = 23, 5, 2
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    ids[:9, 0] = 0   # a hot expert that overflows
+    np.testing.assert_array_equal(O.capacity_keep(ids, E, capacity), py_capacity_keep(ids.tolist(), capacity))
+
+
+def test_capacity_hot_expert_keeps_first_tokens():
+    T, E, C = 12, 4, 5
+    ids = np.zeros((T, 1), dtype=int)            # every token picks expert 0
+    keep = O.capacity_keep(ids, E, C)
+    assert keep[:C, 0].all() and not keep[C:, 0].any()
+    dsp = O.dispatch(ids, E, capacity=C)
+    assert list(dsp["counts"]) == [C, 0, 0, 0]
+    assert list(dsp["perm_src"]) == list(range(C))
+    assert list(dsp["dest"][:, 0]) == list(range(C)) + [-1] * (T - C)
+
+
+def test_capacity_at_or_above_max_count_is_dropless():
+    rng = np.random.default_rng(4)
+    T, E, k = 40, 6, 3
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    cmax = int(np.bincount(ids.reshape(-1)).max())
+    a, b = O.dispatch(ids, E), O.dispatch(ids, E, capacity=cmax)
+    for key in ("counts", "offsets", "perm_src", "dest"):
+        np.testing.assert_array_equal(a[key], b[key])
+    assert (O.dispatch(ids, E, capacity=cmax - 1)["counts"] == np.minimum(np.bincount(ids.reshape(-1)), cmax - 1)).all()
+
+
+def test_capacity_forward_drops_only_refused_assignments():
+    """y with a capacity = shared experts + the accepted routed terms, by loops;
+    a token all of whose picks were refused gets the shared experts alone."""
+    x, W_g, W1, W3, W2 = tiny_layer(11, T=9, d=4, E=4, K_s=1, I=2)
+    ids = np.array([[0, 1]] * 6 + [[2, 3], [0, 1], [1, 2]])
+    g = np.full(ids.shape, 0.5)
+    keep = O.capacity_keep(ids, 4, 5)            # expert 0 and 1 take tokens 0..4 only
+    y = O.moe_forward(x, W1, W3, W2, 1, ids, g, keep=keep)
+    for t in range(9):
+        want = py_ffn(x[t].tolist(), W1[0].tolist(), W3[0].tolist(), W2[0].tolist())
+        for j in range(2):
+            if keep[t, j]:
+                e = 1 + ids[t, j]
+                o = py_ffn(x[t].tolist(), W1[e].tolist(), W3[e].tolist(), W2[e].tolist())
+                want = [a + 0.5 * b for a, b in zip(want, o)]
+        np.testing.assert_allclose(y[t], want, rtol=1e-12, atol=1e-14)
+    assert not keep[5].any() and not keep[7].any()
+    # the grouped path (dispatch -> expert_rows -> combine) gives the same y
+    dsp = O.dispatch(ids, 4, capacity=5)
+    rows = O.expert_rows(x, W1, W3, W2, 1, dsp["perm_src"], dsp["offsets"], 2)
+    np.testing.assert_allclose(O.combine(rows, dsp["dest"], g, 1, 9), y, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- GShard ReLU experts
+
+def test_relu_layer_matches_plain_loops():
+    """wo . ReLU(wi . x) experts ([MoE-notes] section 3) through the whole layer."""
+    x, W_g, W1, W3, W2 = tiny_layer(12, T=6, d=5, E=5, K_s=1, I=3)
+    r = O.route(x, W_g, 2)
+    y = O.moe_forward(x, W1, None, W2, 1, r["ids"], r["gates"], act="relu")
+    for t in range(6):
+        def relu_ffn(e):
+            h = [max(0.0, sum(W1[e][i][c] * x[t][c] for c in range(5))) for i in range(3)]
+            return [sum(W2[e][o][i] * h[i] for i in range(3)) for o in range(5)]
+        want = relu_ffn(0)
+        for gj, e in zip(r["gates"][t], r["ids"][t]):
+            want = [a + gj * b for a, b in zip(want, relu_ffn(1 + e))]
+        np.testing.assert_allclose(y[t], want, rtol=1e-12, atol=1e-14)
+    dsp = O.dispatch(r["ids"], 5)
+    rows = O.expert_rows(x, W1, None, W2, 1, dsp["perm_src"], dsp["offsets"], 2, act="relu")
+    np.testing.assert_allclose(O.combine(rows, dsp["dest"], r["gates"], 1, 6), y, rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------- statistics
+
+def test_logsumexp_and_probability_sums_closed_forms():
+    z = np.full((3, 8), 1.5)
+    np.testing.assert_allclose(O.logsumexp(z), 1.5 + math.log(8), rtol=1e-15)
+    np.testing.assert_allclose(O.prob_column_sums(z), np.full(8, 3 / 8), rtol=1e-15)
+    z = np.array([[0.0, math.log(3.0)], [math.log(2.0), math.log(2.0)]])
+    np.testing.assert_allclose(O.logsumexp(z), [math.log(4.0), math.log(4.0)], rtol=1e-15)
+    np.testing.assert_allclose(O.prob_column_sums(z), [0.25 + 0.5, 0.75 + 0.5], rtol=1e-15)
+    rng = np.random.default_rng(3)
+    z = rng.standard_normal((50, 7)) * 3
+    assert O.prob_column_sums(z).sum() == pytest.approx(50.0, rel=1e-13)   # each row of s sums to 1
+    assert np.mean(O.logsumexp(z) ** 2) == pytest.approx(O.router_z_loss(z), rel=1e-13)
+
 
 def test_cv_squared_hand_values():
     assert O.cv_squared([1, 1, 1, 1]) == 0.0
