@@ -58,19 +58,20 @@ def dist_env():
     return world, rank, local
 
 
-def kernel_flops(w) -> dict:
-    """Algorithmic FLOPs per launch of each kernel (expected rows from routing:
-    T*k routed + K_s*T shared; every row does d x I products)."""
-    rows = w.T * w.top_k + w.n_shared * w.T
+def kernel_flops(w, kept: int) -> dict:
+    """Algorithmic FLOPs per launch of each kernel: `kept` routed rows (T*k
+    when dropless, fewer under an expert capacity) + K_s*T shared rows; each
+    row does one d x I product per expert weight matrix."""
+    rows = kept + w.n_shared * w.T
     return {"router": 2.0 * w.T * w.d * w.n_routed * (2 if w.noisy else 1),
-            "gate_up": 4.0 * rows * w.d * w.d_ff,
+            "gate_up": 2.0 * (w.n_mats - 1) * rows * w.d * w.d_ff,
             "down": 2.0 * rows * w.d * w.d_ff}
 
 
 def algorithmic_bytes(w, touched_experts: int) -> float:
     """Touched expert weights + W_g (+ W_noise) + x + y (+ eps): the method's own traffic."""
     act = 4 if w.fp32 else 2
-    wts = touched_experts * 3 * w.d * w.d_ff * act
+    wts = touched_experts * w.n_mats * w.d * w.d_ff * act
     router = w.d * w.n_routed * 4 * (2 if w.noisy else 1)
     xy = 2 * w.T * w.d * act
     eps = w.T * w.n_routed * 4 if w.noisy else 0
@@ -294,6 +295,7 @@ def main():
                                       layer.W1, layer.W3, layer.W2, workspace=layer.workspace,
                                       routing=True)
     touched = int((counts > 0).sum().item()) + w.n_shared
+    kept = int(counts.sum().item())   # routed rows computed (T*k unless an expert capacity dropped some)
     x_host_bytes = inp["x"].numel() * inp["x"].element_size()
     eps_bytes = inp["eps"].numel() * 4 if inp["eps"] is not None else 0
     y_bytes = w.T * w.d * layer.y.element_size()
@@ -304,13 +306,13 @@ def main():
         return 0
 
     pk, pk_kind = peaks()
-    kf = kernel_flops(w)
+    kf = kernel_flops(w, kept)
     gu_s = stage_ms["gate_up"] / 1e3
     gu_tflops = kf["gate_up"] / gu_s / 1e12
     peak = pk["bf16_tflops"]
     src = os.path.join(ROOT, "mixture_experts_layer_91_b300", "csrc", "gemm_tc.cuh")
     tr = ncu_traffic(src)
-    flops = w.flops()
+    flops = kf["router"] + kf["gate_up"] + kf["down"]
     tokens_per_s = world * w.T / (ms_step / 1e3)
     tflops = world * flops / (ms_step / 1e3) / 1e12
     ab = algorithmic_bytes(w, touched)
@@ -328,6 +330,7 @@ def main():
         "config": {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
                    "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
                    "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
+                   "expert": w.act, "capacity": w.capacity or None,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {ab / 2**20:.0f} MiB of weights+activations per step"},
         "tflops": tflops,

@@ -74,7 +74,38 @@ typedef struct {
   int32_t renormalize; /* 1: gates divided by their sum over the selected set    */
   int32_t gate;        /* moe_gate                                               */
   int32_t act_dtype;   /* moe_dtype                                              */
+  int32_t capacity;    /* max assignments an expert accepts, 0 = no limit        */
+  int32_t expert_act;  /* moe_expert_act                                         */
 } moe_config;
+
+typedef enum {
+  MOE_ACT_SWIGLU = 0,  /* FFN(u) = W2 (silu(W1 u) * (W3 u))                       */
+  MOE_ACT_RELU = 1     /* FFN(u) = W2 ReLU(W1 u) (GShard's wo.ReLU(wi.x)); W3 unused */
+} moe_expert_act;
+
+/*
+ * Expert capacity ("Mixture of Experts" notes, section 3, GShard expert
+ * capacity; section 4, Switch capacity factor): when capacity > 0, expert e
+ * accepts the first `capacity` assignments that select it, in ascending flat
+ * assignment index t*k + j (a running counter c_e per expert); later ones are
+ * dropped: they take no row, their dest is -1, and they add nothing to y (the
+ * token's other experts, the shared experts and the caller's residual still
+ * do). The gate values in topk_w are not changed. A Switch-style capacity
+ * factor f gives capacity = ceil(f * T * k / N_r), computed by the caller.
+ * The DeepSeekMoE layer itself is dropless (capacity = 0).
+ */
+
+/* Optional per-call router statistics (moe_route); NULL members are skipped.
+ * Balance losses are formed from them by the caller:
+ *   z-loss ("Mixture of Experts" notes, section 5, ST-MoE) = mean_t lse[t]^2;
+ *   P_i (DeepSeekMoE translation, section 3.3, eq (14)) = prob_sum[i] / T;
+ *   Importance_i ("Mixture of Experts" notes, section 2) = gate_sum[i];
+ *   f_i (eq (13)) from the per-expert counts of moe_permute. */
+typedef struct {
+  float* lse;          /* [T]   log sum_i exp(x W_g)_i over the routed experts      */
+  float* prob_sum;     /* [N_r] sum over tokens of the softmax probabilities s_i   */
+  float* gate_sum;     /* [N_r] sum over tokens of the gate values g_i (0 if not selected) */
+} moe_router_stats;
 
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
@@ -102,6 +133,8 @@ size_t moe_route_workspace_size(const moe_config* cfg);
  *                                    ties to the lowest index
  *   topk_w   [T, k]   fp32   (out)   gate values g_{i,t} of those experts
  *   logits   [T, N_r] fp32 or NULL (out) the plain logits x W_g
+ *   stats    moe_router_stats or NULL (out) per-token logsumexp and per-expert
+ *                                    sums of s and g (summed with fp32 atomics)
  *   workspace, ws_bytes              scratch, >= moe_route_workspace_size()
  *                                    (may be NULL when that is 0)
  * The logits are an fp32-accurate dot product of the stored inputs. bf16
@@ -113,6 +146,7 @@ size_t moe_route_workspace_size(const moe_config* cfg);
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g,
                      const float* W_noise, const float* eps, const float* bias,
                      int32_t* topk_ids, float* topk_w, float* logits,
+                     const moe_router_stats* stats,
                      void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of scratch moe_permute needs (per-block histograms and ranks). */
@@ -134,7 +168,9 @@ size_t moe_permute_workspace_size(const moe_config* cfg);
  *   dest      [T, k]       int32 (out) grouped row of each assignment
  *   perm_src  [T*k]        int32 (out) flat assignment index of each grouped row
  *   x_perm    [T*k, d]     act_dtype (out) x_perm[dest[t,j]] = x[t]
- * Ids outside [0, N_r) are skipped and raise MOE_ERR_DEVICE_INDEX.
+ * Ids outside [0, N_r) are skipped and raise MOE_ERR_DEVICE_INDEX. With
+ * cfg->capacity > 0, counts are the accepted counts and dropped assignments
+ * get dest = -1 and no row.
  */
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_ids,
                        void* workspace, size_t ws_bytes, int32_t* counts, int32_t* offsets,
@@ -185,6 +221,7 @@ size_t moe_expert_ffn_workspace_size(const moe_config* cfg);
  *   x_perm    [T*k, d]      act_dtype  grouped rows from moe_permute
  *   offsets   [N_r + 1]     int32      group bounds from moe_permute
  *   W1, W3    [K_s+N_r, I, d] act_dtype; W2 [K_s+N_r, d, I] act_dtype
+ *             (W3 may be NULL when cfg->expert_act = MOE_ACT_RELU)
  *   workspace, ws_bytes                scratch, >= moe_expert_ffn_workspace_size()
  *   out_rows  [K_s*T + T*k, d] fp32 (out): row i*T + t = FFN_i(x_t) for shared
  *             expert i; row K_s*T + r = FFN_{K_s+e}(x_perm[r]) for r in group e.
@@ -200,6 +237,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x, const void* x_pe
  * moe_combine -- gate-weighted combine back to token order (eq (9) without
  * the residual; "Mixture of Experts" notes, section 3, y_s = sum_e G_{s,e} FFN_e(x_s)):
  *   y_t = sum_{i<K_s} out_rows[i*T + t] + sum_j topk_w[t,j] out_rows[K_s*T + dest[t,j]]
+ *   (terms with dest[t,j] = -1, dropped by an expert's capacity, are skipped)
  *   out_rows [K_s*T + T*k, d] fp32; dest [T, k] int32; topk_w [T, k] fp32;
  *   y [T, d] act_dtype (out). Summed in fp32 in a fixed order (deterministic).
  */

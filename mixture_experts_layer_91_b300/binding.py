@@ -44,18 +44,27 @@ class MoeError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)}")
 
 
+MOE_ACT_SWIGLU, MOE_ACT_RELU = 0, 1
+
+
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("n_routed", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("gate", ctypes.c_int32),
-                ("act_dtype", ctypes.c_int32)]
+                ("act_dtype", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("expert_act", ctypes.c_int32)]
+
+
+class RouterStats(ctypes.Structure):
+    _fields_ = [("lse", ctypes.c_void_p), ("prob_sum", ctypes.c_void_p), ("gate_sum", ctypes.c_void_p)]
 
 
 def config(w: Workload, T: int | None = None) -> MoeConfig:
     return MoeConfig(T=w.T if T is None else T, d=w.d, n_routed=w.n_routed, n_shared=w.n_shared,
                      top_k=w.top_k, d_ff=w.d_ff, renormalize=int(w.renormalize or w.noisy),
                      gate=MOE_GATE_NOISY if w.noisy else MOE_GATE_SOFTMAX,
-                     act_dtype=MOE_DT_F32 if w.fp32 else MOE_DT_BF16)
+                     act_dtype=MOE_DT_F32 if w.fp32 else MOE_DT_BF16, capacity=w.capacity,
+                     expert_act=MOE_ACT_RELU if w.act == "relu" else MOE_ACT_SWIGLU)
 
 
 def load(path: str = _LIB_PATH) -> ctypes.CDLL:
@@ -73,7 +82,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "moe_version": (ctypes.c_int, []),
             "moe_route_workspace_size": (SZ, [C]),
-            "moe_route": (I32, [C, P, P, P, P, P, P, P, P, P, SZ, P]),
+            "moe_route": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P]),
             "moe_permute_workspace_size": (SZ, [C]),
             "moe_permute": (I32, [C, P, P, P, SZ, P, P, P, P, P, P]),
             "moe_permute_static": (I32, [C, P, P, P, P, P, P, P, P]),
@@ -144,21 +153,38 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
 
 
-def route(cfg, x, W_g, W_noise=None, eps=None, bias=None, *, want_logits=False, stream=None):
+def route(cfg, x, W_g, W_noise=None, eps=None, bias=None, *, want_logits=False, want_stats=False,
+          stream=None):
+    """moe_route. Returns (ids, gates), plus logits [T, E] with want_logits,
+    plus a dict of router statistics (lse [T], prob_sum [E], gate_sum [E])
+    with want_stats."""
     lib = load()
     T, k, E = cfg.T, cfg.top_k, cfg.n_routed
     dev = x.device
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     w = torch.empty(T, k, dtype=torch.float32, device=dev)
     logits = torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None
+    stats = stats_c = None
+    if want_stats:
+        stats = {"lse": torch.empty(T, dtype=torch.float32, device=dev),
+                 "prob_sum": torch.empty(E, dtype=torch.float32, device=dev),
+                 "gate_sum": torch.empty(E, dtype=torch.float32, device=dev)}
+        stats_c = RouterStats(stats["lse"].data_ptr(), stats["prob_sum"].data_ptr(),
+                              stats["gate_sum"].data_ptr())
     ws = _workspace(route_workspace_size(cfg), dev)
     st = lib.moe_route(ctypes.byref(cfg), _ptr(x, act_dtype(cfg), "x"), _ptr(W_g, torch.float32, "W_g"),
                        _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
                        _ptr(bias, torch.float32, "bias", True), ids.data_ptr(), w.data_ptr(),
-                       logits.data_ptr() if logits is not None else None, ws.data_ptr(), ws.numel(),
+                       logits.data_ptr() if logits is not None else None,
+                       ctypes.byref(stats_c) if stats_c is not None else None, ws.data_ptr(), ws.numel(),
                        _stream(stream))
     _check(st, "moe_route")
-    return (ids, w, logits) if want_logits else (ids, w)
+    out = (ids, w)
+    if want_logits:
+        out = out + (logits,)
+    if want_stats:
+        out = out + (stats,)
+    return out
 
 
 def permute(cfg, x, topk_ids, *, stream=None) -> dict:
@@ -205,7 +231,8 @@ def expert_ffn(cfg, x, x_perm, offsets, W1, W3, W2, *, stream=None) -> torch.Ten
     ws = _workspace(expert_ffn_workspace_size(cfg), x.device)
     out = torch.empty(K_s * T + T * k, d, dtype=torch.float32, device=x.device)
     st = lib.moe_expert_ffn(ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(x_perm, dt, "x_perm"),
-                            _ptr(offsets, torch.int32, "offsets"), _ptr(W1, dt, "W1"), _ptr(W3, dt, "W3"),
+                            _ptr(offsets, torch.int32, "offsets"), _ptr(W1, dt, "W1"),
+                            _ptr(W3, dt, "W3", cfg.expert_act == MOE_ACT_RELU),
                             _ptr(W2, dt, "W2"), ws.data_ptr(), ws.numel(), out.data_ptr(), _stream(stream))
     _check(st, "moe_expert_ffn")
     return out
@@ -238,7 +265,8 @@ def forward(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, *, workspace=None, y=No
         counts = torch.empty(cfg.n_routed, dtype=torch.int32, device=dev)
     st = lib.moe_forward(ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(W_g, torch.float32, "W_g"),
                          _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
-                         _ptr(bias, torch.float32, "bias", True), _ptr(W1, dt, "W1"), _ptr(W3, dt, "W3"),
+                         _ptr(bias, torch.float32, "bias", True), _ptr(W1, dt, "W1"),
+                         _ptr(W3, dt, "W3", cfg.expert_act == MOE_ACT_RELU),
                          _ptr(W2, dt, "W2"), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                          _ptr(y, dt, "y"), ids.data_ptr() if routing else None,
                          w.data_ptr() if routing else None, counts.data_ptr() if routing else None,
@@ -262,7 +290,8 @@ def forward_profiled(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, *, workspace, 
     st = lib.moe_forward_profiled(ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(W_g, torch.float32, "W_g"),
                                   _ptr(W_noise, torch.float32, "W_noise", True),
                                   _ptr(eps, torch.float32, "eps", True), _ptr(bias, torch.float32, "bias", True),
-                                  _ptr(W1, dt, "W1"), _ptr(W3, dt, "W3"), _ptr(W2, dt, "W2"),
+                                  _ptr(W1, dt, "W1"), _ptr(W3, dt, "W3", cfg.expert_act == MOE_ACT_RELU),
+                                  _ptr(W2, dt, "W2"),
                                   _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                   _ptr(y, dt, "y"), None, None, None, _stream(stream), arr)
     _check(st, "moe_forward_profiled")
@@ -296,7 +325,7 @@ class MoELayer:
         self.W_noise = inputs["W_noise"].to(dev) if inputs["W_noise"] is not None else None
         self.bias = inputs["bias"].to(dev) if inputs["bias"] is not None else None
         self.W1 = inputs["W1"].to(dev)
-        self.W3 = inputs["W3"].to(dev)
+        self.W3 = inputs["W3"].to(dev) if inputs["W3"] is not None else None
         self.W2 = inputs["W2"].to(dev)
         self.workspace = _workspace(workspace_size(self.cfg), dev)
         self.y = torch.empty(w.T, w.d, dtype=act_dtype(self.cfg), device=dev)

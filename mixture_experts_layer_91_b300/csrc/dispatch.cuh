@@ -7,8 +7,9 @@
 //   count_kernel   per block of 1024 assignments: per-expert counts and the
 //                  rank of every assignment among earlier ones of its expert
 //                  (warp match_any + popc, stable in flat index t*k + j);
-//   scan_kernel    one CTA: per-expert totals, offsets (exclusive scan),
-//                  per-block bases, and the GEMM group plan;
+//   scan_kernel    one CTA: per-expert totals, accepted counts (capped by
+//                  the expert capacity, if any), offsets (exclusive scan),
+//                  per-block rank bases, and the GEMM group plan;
 //   scatter_kernel dest / perm_src and the row gather x -> x_perm (16-byte
 //                  vectors, one warp per assignment).
 // combine_kernel is the gate-weighted sum back to token order (DeepSeekMoE
@@ -122,11 +123,14 @@ __device__ void plan_groups(const int32_t* offsets, int32_t E, int32_t K_s, int6
 
 constexpr int kScanThreads = 1024;
 
-// One CTA. blk_hist [nblk][E]: per-block counts in, per-block bases out
-// (offsets[e] + counts of expert e in earlier blocks).
+// One CTA. blk_hist [nblk][E]: per-block counts in, per-block rank bases out
+// (the assignments of expert e in earlier blocks). counts/offsets are the
+// accepted counts: min(total, capacity) when capacity > 0 (GShard's expert
+// capacity; the first `capacity` assignments in flat order are the accepted ones).
 __global__ void __launch_bounds__(kScanThreads)
-    scan_kernel(int32_t* __restrict__ blk_hist, int32_t nblk, int32_t E, int32_t* __restrict__ counts,
-                int32_t* __restrict__ offsets, int32_t K_s, int64_t T, PlanOut plan, int32_t with_plan) {
+    scan_kernel(int32_t* __restrict__ blk_hist, int32_t nblk, int32_t E, int32_t capacity,
+                int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t K_s, int64_t T,
+                PlanOut plan, int32_t with_plan) {
   __shared__ int32_t tot[kMaxGroups + 1];
   __shared__ int32_t part[kScanThreads];
   // split the block range of each expert over `parts` threads
@@ -150,17 +154,16 @@ __global__ void __launch_bounds__(kScanThreads)
   if (threadIdx.x == 0) {
     int32_t r = 0;
     for (int i = 0; i < E; ++i) {
-      const int32_t c = tot[i];
+      const int32_t c = capacity > 0 ? min(tot[i], capacity) : tot[i];
       counts[i] = c;
       offsets[i] = r;
-      tot[i] = r;
       r += c;
     }
     offsets[E] = r;
   }
   __syncthreads();
   if (active) {
-    int32_t base = tot[e];
+    int32_t base = 0;
     for (int j = 0; j < pi; ++j) base += part[j * E + e];
     for (int b = b0; b < b1; ++b) {
       const int64_t i = static_cast<int64_t>(b) * E + e;
@@ -188,6 +191,7 @@ template <typename TX>
 __global__ void __launch_bounds__(256)
     scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int32_t k, int32_t E,
                    const int32_t* __restrict__ blk_base, const int32_t* __restrict__ local_rank,
+                   const int32_t* __restrict__ offsets, int32_t capacity,
                    const TX* __restrict__ x, int32_t d, int32_t* __restrict__ dest,
                    int32_t* __restrict__ perm_src, TX* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
@@ -200,7 +204,13 @@ __global__ void __launch_bounds__(256)
       if (lane == 0) dest[a] = -1;
       continue;
     }
-    const int32_t r = __ldg(blk_base + (a / kCountBlock) * E + e) + __ldg(local_rank + a);
+    // rank of this assignment among those of expert e (ascending flat index)
+    const int32_t rk = __ldg(blk_base + (a / kCountBlock) * E + e) + __ldg(local_rank + a);
+    if (capacity > 0 && rk >= capacity) {   // refused by the expert's capacity
+      if (lane == 0) dest[a] = -1;
+      continue;
+    }
+    const int32_t r = __ldg(offsets + e) + rk;
     if (lane == 0) {
       dest[a] = r;
       perm_src[r] = static_cast<int32_t>(a);

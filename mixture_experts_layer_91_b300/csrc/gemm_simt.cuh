@@ -4,8 +4,8 @@
 // rounding), so they run as plain FMA tiles: 32 rows x 64 columns per CTA,
 // K staged through shared memory in chunks of 32. Same group plan, same
 // padded H layout and same epilogues as the tensor-core kernels
-// (gate-up: h = silu(x W1^T) * (x W3^T); down: rows or gate-weighted
-// scatter-add into the token's output row).
+// (gate-up: h = silu(x W1^T) * (x W3^T), or relu(x W1^T) for GShard ReLU
+// experts; down: rows or gate-weighted scatter-add into the token's output row).
 #pragma once
 
 #include "common.cuh"
@@ -26,6 +26,7 @@ struct SimtArgs {
   float* out;         // down: y (scatter) or out_rows (store), row width n_out
   const int32_t* perm_src;
   const float* topk_w;
+  int32_t relu;       // gate-up: GShard ReLU experts, h = relu(x W1^T) (W3 unused)
 };
 
 template <int MODE>
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(kSimtThreads) grouped_gemm_simt(const SimtArgs
       }
 #pragma unroll
       for (int m = 0; m < NB; ++m) {
+        if (m == 1 && p.relu) continue;
         const float* B = (m == 0 ? p.b0 : p.b1) + boff;
         for (int i = tid; i < kSimtBN * kSimtBK; i += kSimtThreads) {
           const int r = i / kSimtBK, kk = i % kSimtBK;
@@ -105,7 +107,8 @@ __global__ void __launch_bounds__(kSimtThreads) grouped_gemm_simt(const SimtArgs
         float* h = p.h_out + (hrow0 + r) * p.n_out + n0;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (4 * tx + j < ncols) h[4 * tx + j] = silu_f(acc[0][i][j]) * acc[1][i][j];
+          if (4 * tx + j < ncols)
+            h[4 * tx + j] = p.relu ? fmaxf(acc[0][i][j], 0.f) : silu_f(acc[0][i][j]) * acc[1][i][j];
       } else {
         int64_t orow;
         float gate = 1.f;

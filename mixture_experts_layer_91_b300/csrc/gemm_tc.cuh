@@ -22,7 +22,8 @@
 //               fp32 combine accumulator while the first MMAs run) then
 //               tcgen05.ld of the accumulator (each warp owns one
 //               32-lane quarter), then
-//                 gate-up : h = silu(acc[:, 0:128]) * acc[:, 128:256] -> bf16,
+//                 gate-up : h = silu(acc[:, 0:128]) * acc[:, 128:256] -> bf16
+//                           (GShard ReLU experts: h = relu(acc[:, 0:256])),
 //                           staged in shared memory, TMA-stored to H;
 //                 down    : acc * gate, transposed in registers so each warp
 //                           instruction adds one 128-byte row segment
@@ -79,6 +80,7 @@ struct TcArgs {
   int32_t fold_mt;          // down scatter with K_s > 0: m-tiles per shared group, else 0
   float4* zero_out;         // gate-up: buffer the epilogue warps clear (fp32 combine accumulator)
   int64_t zero_n4;          // its size in float4
+  int32_t relu;             // gate-up: GShard ReLU experts (h = relu(W1 x); the B tile is 256 W1 rows)
 };
 
 struct TcMaps {
@@ -210,7 +212,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           a_y = c.mt * kTcBM;   // padded H row of this m-tile
         }
-        const int32_t b_y = c.g * p.b_rows + c.nt * (MODE == kEpiSwiGLU ? kTcBN / 2 : kTcBN);
+        // gate-up: 128 W1 rows over the same 128 W3 rows (SwiGLU), or 256 W1 rows (ReLU)
+        const int32_t b_y = c.g * p.b_rows + c.nt * (MODE == kEpiSwiGLU && !p.relu ? kTcBN / 2 : kTcBN);
         for (int32_t kb = 0, e = 0, kx = 0; kb < c.nk; ++kb, ++it) {
           // folded shared group: k-block kb is block kx of shared expert e
           if (kx == nk) { kx = 0; ++e; }
@@ -224,7 +227,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (MODE == kEpiSwiGLU) {
             tma_load_2d(sa, amap, full, kb * kTcBK, a_y);
             tma_load_2d(sb, &maps.b0, full, kb * kTcBK, b_y);
-            tma_load_2d(sb + kTileBBytes / 2, &maps.b1, full, kb * kTcBK, b_y);
+            // (ReLU: maps.b1 is also W1, and the second half is its next 128 rows)
+            tma_load_2d(sb + kTileBBytes / 2, &maps.b1, full, kb * kTcBK, b_y + (p.relu ? kTcBN / 2 : 0));
           } else {
             // expert e's H rows start at its own m-tiles; its W2 rows at e * d
             tma_load_2d(sa, amap, full, kx * kTcBK, a_y + e * p.fold_mt * kTcBM);
@@ -321,18 +325,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       if (MODE == kEpiSwiGLU) {
         const uint32_t buf0 = sStore + ew * 2 * kStoreBoxBytes;
+        // SwiGLU: 128 output columns (gate | up halves); ReLU: 256
+        const int nchunk = p.relu ? kTcBN / 32 : kTcBN / 2 / 32;
+        const int32_t col0 = c.nt * (p.relu ? kTcBN : kTcBN / 2);
 #pragma unroll 1
-        for (int cc = 0; cc < kTcBN / 2 / 32; ++cc, ++nstore) {
+        for (int cc = 0; cc < nchunk; ++cc, ++nstore) {
           uint32_t g[32], u[32];
           tmem_ld_32x32b_x32(tacc + cc * 32, g);
-          tmem_ld_32x32b_x32(tacc + kTcBN / 2 + cc * 32, u);
+          if (!p.relu) tmem_ld_32x32b_x32(tacc + kTcBN / 2 + cc * 32, u);
           tmem_ld_wait();
           uint32_t hp[16];
+          if (p.relu) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-            const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-            hp[j] = pack_bf16x2(h0, h1);
+            for (int j = 0; j < 16; ++j)
+              hp[j] = pack_bf16x2(fmaxf(__uint_as_float(g[2 * j]), 0.f), fmaxf(__uint_as_float(g[2 * j + 1]), 0.f));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+              const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+              hp[j] = pack_bf16x2(h0, h1);
+            }
           }
           const uint32_t buf = buf0 + (nstore & 1u) * kStoreBoxBytes;
           if (nstore >= 2) {  // the store issued two boxes ago read this buffer
@@ -350,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&maps.out, buf, c.nt * (kTcBN / 2) + cc * 32, c.mt * kTcBM + q * 32);
+            tma_store_2d(&maps.out, buf, col0 + cc * 32, c.mt * kTcBM + q * 32);
             bulk_commit();
           }
         }

@@ -24,7 +24,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kVersion = (1 << 16) | 1;
+constexpr int kVersion = (2 << 16) | 0;
 constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
@@ -42,6 +42,8 @@ moe_status check_config(const moe_config* c) {
   if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
   // noisy top-k always renormalises over the kept entries (softmax of KeepTopK)
   if (c->gate == MOE_GATE_NOISY && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (c->expert_act != MOE_ACT_SWIGLU && c->expert_act != MOE_ACT_RELU) return MOE_ERR_INVALID_ARG;
   if (c->d % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
   const int cols = c->gate == MOE_GATE_NOISY ? 2 * c->n_routed : c->n_routed;
   if (cols > 256 || c->top_k > 32 || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
@@ -244,7 +246,8 @@ moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : M
 // ---------------------------------------------------------------------------
 moe_status launch_route(const moe_config* c, const void* x, const float* W_g, const float* W_noise,
                         const float* eps, const float* bias, int32_t* ids, float* w, float* logits,
-                        float* zero_rows, int sm_count, void* planes, cudaStream_t st) {
+                        float* zero_rows, int sm_count, void* planes, cudaStream_t st,
+                        const moe_router_stats* stats = nullptr) {
   RouterArgs a;
   a.x = x;
   a.W_g = W_g;
@@ -263,6 +266,15 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   a.noisy = c->gate == MOE_GATE_NOISY;
   a.zero_width = c->d;
   a.w_vec4 = (c->n_routed % 4 == 0) && aligned16(W_g) && (W_noise == nullptr || aligned16(W_noise));
+  a.lse = stats ? stats->lse : nullptr;
+  a.prob_sum = stats ? stats->prob_sum : nullptr;
+  a.gate_sum = stats ? stats->gate_sum : nullptr;
+  if (c->T > 0) {   // the per-expert sums are accumulated with atomics
+    if (a.prob_sum && cudaMemsetAsync(a.prob_sum, 0, sizeof(float) * c->n_routed, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (a.gate_sum && cudaMemsetAsync(a.gate_sum, 0, sizeof(float) * c->n_routed, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   const int cols = a.noisy ? 2 * a.E : a.E;
   const int np = router_tc_np(c);
   if (np > 0) {
@@ -335,18 +347,18 @@ moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void
     MOE_TRY(last_launch());
   }
   PlanOut none{};
-  scan_kernel<<<1, kScanThreads, 0, st>>>(blk, static_cast<int32_t>(nblk), E, counts, offsets,
-                                          c->n_shared, c->T, plan ? *plan : none, plan ? 1 : 0);
+  scan_kernel<<<1, kScanThreads, 0, st>>>(blk, static_cast<int32_t>(nblk), E, c->capacity, counts,
+                                          offsets, c->n_shared, c->T, plan ? *plan : none, plan ? 1 : 0);
   MOE_TRY(last_launch());
   if (n > 0) {
     const int64_t want = (n + 7) / 8;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, 16ll * ds->sm_count));
     if (c->act_dtype == MOE_DT_BF16)
       scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-          ids, n, c->top_k, E, blk, rank, static_cast<const __nv_bfloat16*>(x), c->d, dest,
-          perm_src, static_cast<__nv_bfloat16*>(x_perm));
+          ids, n, c->top_k, E, blk, rank, offsets, c->capacity, static_cast<const __nv_bfloat16*>(x),
+          c->d, dest, perm_src, static_cast<__nv_bfloat16*>(x_perm));
     else
-      scatter_kernel<float><<<grid, 256, 0, st>>>(ids, n, c->top_k, E, blk, rank,
+      scatter_kernel<float><<<grid, 256, 0, st>>>(ids, n, c->top_k, E, blk, rank, offsets, c->capacity,
                                                   static_cast<const float*>(x), c->d, dest,
                                                   perm_src, static_cast<float*>(x_perm));
     MOE_TRY(last_launch());
@@ -373,7 +385,8 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     MOE_TRY(make_map(&gu.a1, x_perm, bf, 2, d, n_assign(c), kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B));
     MOE_TRY(make_map(&gu.b0, W1, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B));
-    MOE_TRY(make_map(&gu.b1, W3, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2,
+    const bool relu = c->expert_act == MOE_ACT_RELU;   // W3 unused: both B halves come from W1
+    MOE_TRY(make_map(&gu.b1, relu ? W1 : W3, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B));
     MOE_TRY(make_map(&gu.out, H, bf, 2, I, P, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
     MOE_TRY(make_map(&dn.a0, H, bf, 2, I, P, kTcBK, kTcBM, CU_TENSOR_MAP_SWIZZLE_128B));
@@ -393,7 +406,8 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     const unsigned grid = static_cast<unsigned>(ds->sm_count);
 
     a.K = d;
-    a.n_tiles = (I + kTcBN / 2 - 1) / (kTcBN / 2);
+    a.relu = relu ? 1 : 0;
+    a.n_tiles = relu ? (I + kTcBN - 1) / kTcBN : (I + kTcBN / 2 - 1) / (kTcBN / 2);
     a.b_rows = I;
     a.n_out = I;
     a.zero_out = reinterpret_cast<float4*>(zero);
@@ -433,6 +447,7 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
   a.a1 = static_cast<const float*>(x_perm);
   a.b0 = static_cast<const float*>(W1);
   a.b1 = static_cast<const float*>(W3);
+  a.relu = c->expert_act == MOE_ACT_RELU ? 1 : 0;
   a.h_out = static_cast<float*>(H);
   grouped_gemm_simt<kEpiSwiGLU><<<grid, kSimtThreads, 0, st>>>(a);
   MOE_TRY(last_launch());
@@ -513,7 +528,8 @@ size_t moe_route_workspace_size(const moe_config* cfg) {
 
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
                      const float* eps, const float* bias, int32_t* topk_ids, float* topk_w,
-                     float* logits, void* workspace, size_t ws_bytes, void* stream) {
+                     float* logits, const moe_router_stats* stats, void* workspace, size_t ws_bytes,
+                     void* stream) {
   MOE_TRY(check_config(cfg));
   const bool noisy = cfg->gate == MOE_GATE_NOISY;
   if (cfg->T > 0 && (x == nullptr || W_g == nullptr || topk_ids == nullptr || topk_w == nullptr))
@@ -526,7 +542,8 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, con
   DeviceState* ds;
   MOE_TRY(device_state(&ds));
   return launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, topk_ids,
-                      topk_w, logits, nullptr, ds->sm_count, workspace, static_cast<cudaStream_t>(stream));
+                      topk_w, logits, nullptr, ds->sm_count, workspace, static_cast<cudaStream_t>(stream),
+                      stats);
 }
 
 size_t moe_permute_workspace_size(const moe_config* cfg) {
@@ -582,7 +599,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x, const void* x_pe
                           void* workspace, size_t ws_bytes, float* out_rows, void* stream) {
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
-  if (x == nullptr || x_perm == nullptr || offsets == nullptr || W1 == nullptr || W3 == nullptr ||
+  const bool need_w3 = cfg->expert_act == MOE_ACT_SWIGLU;
+  if (x == nullptr || x_perm == nullptr || offsets == nullptr || W1 == nullptr || (need_w3 && W3 == nullptr) ||
       W2 == nullptr || workspace == nullptr || out_rows == nullptr)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) ||
@@ -635,7 +653,8 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   const bool noisy = cfg->gate == MOE_GATE_NOISY;
   if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
-  if (x == nullptr || W_g == nullptr || W1 == nullptr || W3 == nullptr || W2 == nullptr ||
+  const bool need_w3 = cfg->expert_act == MOE_ACT_SWIGLU;
+  if (x == nullptr || W_g == nullptr || W1 == nullptr || (need_w3 && W3 == nullptr) || W2 == nullptr ||
       workspace == nullptr || y == nullptr)
     return MOE_ERR_INVALID_ARG;
   if (noisy && (W_noise == nullptr || eps == nullptr)) return MOE_ERR_INVALID_ARG;

@@ -40,6 +40,11 @@ struct RouterArgs {
   int64_t T;
   int32_t d, E, k, renorm, noisy, zero_width;
   int32_t w_vec4;        // W rows may be copied in 16-byte pieces (E % 4 == 0, aligned)
+  // optional statistics (null = skip): per-token logsumexp of the logits;
+  // per-expert sums over tokens of s and of the gates (added with atomics)
+  float* lse;
+  float* prob_sum;
+  float* gate_sum;
 };
 
 constexpr int kRouterBT = 32;       // tokens per CTA
@@ -295,6 +300,11 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
   const uint32_t crank = cluster_rank();
   const uint32_t csize = cluster_size();
   const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * S::BT;
+  __shared__ float s_prob[EPAD], s_gate[EPAD];   // per-CTA statistic sums
+  for (int c = tid; c < EPAD; c += kRouterThreads) {
+    s_prob[c] = 0.f;
+    s_gate[c] = 0.f;
+  }
 
   // fused clear of the fp32 accumulator rows of these tokens (forward path),
   // shared among the CTAs of the cluster
@@ -380,10 +390,12 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
     const float inv = 1.0f / ssum;
+    if (p.lse != nullptr && lane == 0) p.lse[t] = m + logf(ssum);
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
       const int cc = lane + 32 * i;
       sv[i] *= inv;
+      if (p.prob_sum != nullptr && cc < p.E) atomicAdd(&s_prob[cc], sv[i]);
       if (cc >= p.E) {
         key[i] = -INFINITY;
       } else if (p.noisy) {
@@ -438,6 +450,14 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
       if (p.noisy || p.renorm) g = my_val / sel_sum;
       p.topk_ids[t * p.k + lane] = my_id;
       p.topk_w[t * p.k + lane] = g;
+      if (p.gate_sum != nullptr) atomicAdd(&s_gate[my_id], g);
+    }
+  }
+  if (p.prob_sum != nullptr || p.gate_sum != nullptr) {
+    __syncthreads();
+    for (int c = tid; c < p.E; c += kRouterThreads) {
+      if (p.prob_sum != nullptr) atomicAdd(p.prob_sum + c, s_prob[c]);
+      if (p.gate_sum != nullptr) atomicAdd(p.gate_sum + c, s_gate[c]);
     }
   }
 }

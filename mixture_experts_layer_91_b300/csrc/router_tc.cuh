@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   asm volatile("bar.arrive 1, 160;" ::: "memory");
 
   const int64_t t = t0 + row;
-  if (!ok || t >= p.T) return;
+  if (!ok) return;   // warp-uniform
+  const bool valid = t < p.T;
   const int E = p.E;
 
   // logits row in shared memory (the operand ring is idle now: every load
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   float* Lrow = reinterpret_cast<float*>(gbase) + row * S::LS;
 #pragma unroll
   for (int c = 0; c < NP; ++c) Lrow[c] = acc[c];
-  if (p.logits_out != nullptr)
+  if (p.logits_out != nullptr && valid)
     for (int c = 0; c < E; ++c) p.logits_out[t * E + c] = Lrow[c];
 
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -310,7 +311,22 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
 #pragma unroll
   for (int c = 0; c < NP; ++c)
     if (c < E) sm[c & 3] += expf(acc[c] - m);
-  const float inv = 1.0f / ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+  const float ssum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+  const float inv = 1.0f / ssum;
+  if (p.lse != nullptr && valid) p.lse[t] = m + logf(ssum);
+  if (p.prob_sum != nullptr) {
+    // sum of s over this warp's 32 tokens per expert, then one atomic per warp
+#pragma unroll
+    for (int c = 0; c < NP; ++c) {
+      if (c < E) {   // uniform across the warp
+        float v = valid ? expf(acc[c] - m) * inv : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) atomicAdd(p.prob_sum + c, v);
+      }
+    }
+  }
+  if (!valid) return;
 
   // selection keys, in place; NaN = not selectable
   const float nan = __int_as_float(0x7fffffff);
@@ -358,6 +374,8 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   }
   if (p.noisy || p.renorm)
     for (int r = 0; r < p.k; ++r) p.topk_w[t * p.k + r] /= sel_sum;
+  if (p.gate_sum != nullptr)
+    for (int r = 0; r < p.k; ++r) atomicAdd(p.gate_sum + p.topk_ids[t * p.k + r], p.topk_w[t * p.k + r]);
 }
 
 }  // namespace moe

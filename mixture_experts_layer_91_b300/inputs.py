@@ -5,7 +5,8 @@ Recipe (the same for the CUDA path, its tests and the oracle):
   * x ~ N(0, 1), drawn in fp32 and stored as bf16 (fp32 for fp32 workloads);
   * W_g ~ N(0, 0.02^2) fp32 [d, N_r]; W_noise likewise for the noisy gate;
   * expert weights ~ N(0, 0.02^2): W1, W3 [K_s+N_r, I, d], W2 [K_s+N_r, d, I],
-    stored bf16 (fp32 for fp32 workloads), shared experts first;
+    stored bf16 (fp32 for fp32 workloads), shared experts first (ReLU
+    experts have no W3: that draw is skipped);
   * noisy gate: eps ~ N(0, 1) fp32 [T, N_r], the StandardNormal() draws;
   * selection bias: b_i = 0.05 * r_i^(-1.1), r a seeded permutation of
     1..N_r (a Zipf(1.1) skew over the experts).
@@ -50,7 +51,7 @@ def make_inputs(w: Workload, *, with_experts: bool = True) -> dict:
     if with_experts:
         E, I, d = w.n_experts, w.d_ff, w.d
         out["W1"] = _randn_chunked((E, I, d), g, act)
-        out["W3"] = _randn_chunked((E, I, d), g, act)
+        out["W3"] = _randn_chunked((E, I, d), g, act) if w.act != "relu" else None
         out["W2"] = _randn_chunked((E, d, I), g, act)
     return out
 

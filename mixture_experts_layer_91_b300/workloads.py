@@ -33,6 +33,8 @@ class Workload:
     bias: bool = False          # auxiliary-loss-free selection bias
     fp32: bool = False          # activations and expert weights in fp32 (else bf16)
     seed: int = 91
+    capacity: int = 0           # assignments an expert accepts (0 = dropless)
+    act: str = "swiglu"         # expert FFN: "swiglu" or GShard's "relu" (no W3)
 
     @property
     def n_experts(self) -> int:
@@ -42,11 +44,17 @@ class Workload:
     def n_assign(self) -> int:
         return self.T * self.top_k
 
+    @property
+    def n_mats(self) -> int:
+        """d x I weight matrices per expert: W1, W3, W2 (SwiGLU) or W1, W2 (ReLU)."""
+        return 2 if self.act == "relu" else 3
+
     def flops(self) -> float:
         """Algorithmic FLOPs of one forward: the router x.W_g (twice with the
-        noise projection) plus three d x I products per active expert per token."""
+        noise projection) plus one d x I product per weight matrix per active
+        expert per token (dropless)."""
         router = 2.0 * self.T * self.d * self.n_routed * (2 if self.noisy else 1)
-        ffn = 6.0 * self.T * self.d * self.d_ff * (self.top_k + self.n_shared)
+        ffn = 2.0 * self.n_mats * self.T * self.d * self.d_ff * (self.top_k + self.n_shared)
         return router + ffn
 
     def with_tokens(self, T: int, name: str | None = None) -> "Workload":
@@ -66,7 +74,13 @@ DSMOE_145B = Workload("dsmoe145b_prefill_T32768", T=32768, d=4096, n_routed=128,
                       n_shared=4, top_k=12, d_ff=1024, bias=True, seed=95)
 DSMOE_145B_DECODE = replace(DSMOE_145B, name="dsmoe145b_decode_T64", T=64)
 
-ALL = [TINY_FP32, DSMOE_2B, DSMOE_16B, GSHARD_NOISY, DSMOE_145B, DSMOE_145B_DECODE]
+# GShard's own expert form wo.ReLU(wi.x) on the GShard-style layer (same
+# parameters per expert as its SwiGLU twin minus W3), with a Switch-style
+# expert capacity of 1.25 x the mean load: ceil(1.25 * T * k / E).
+GSHARD_RELU_CAP = replace(GSHARD_NOISY, name="gshard_relu_cap1.25_T16384", act="relu",
+                          capacity=-(-5 * 16384 * 2 // (4 * 16)), seed=96)
+
+ALL = [TINY_FP32, DSMOE_2B, DSMOE_16B, GSHARD_NOISY, DSMOE_145B, DSMOE_145B_DECODE, GSHARD_RELU_CAP]
 BY_NAME = {w.name: w for w in ALL}
 
 # the layer the throughput headline is quoted on: the 16B-shaped layer at 16K tokens

@@ -28,16 +28,28 @@ DEV = "cuda"
 # bf16 tokens with more than 128 router columns take the CUDA-core router
 WIDE_ROUTER = workloads.Workload("wide_router_bf16_T777", T=777, d=512, n_routed=160, n_shared=1,
                                  top_k=8, d_ff=128, seed=17)
+# GShard ReLU experts under an expert capacity (mean load 37.5 per expert): some overflow
+GSHARD_RELU_SMALL = workloads.Workload("gshard_relu_cap40_T300", T=300, d=512, n_routed=16, n_shared=0,
+                                       top_k=2, d_ff=320, renormalize=True, noisy=True, seed=21,
+                                       capacity=40, act="relu")
+# shared + routed SwiGLU experts under a capacity below the mean load (333*6/64 = 31.2)
+DSMOE_16B_CAP = workloads.DSMOE_16B.with_tokens(333, "dsmoe16b_cap28_T333")
+DSMOE_16B_CAP = workloads.replace(DSMOE_16B_CAP, capacity=28)
+TINY_RELU = workloads.replace(workloads.TINY_FP32, name="tiny_fp32_relu_T256", act="relu", seed=23)
 SMALL = [
     workloads.TINY_FP32,
+    TINY_RELU,
     WIDE_ROUTER,
+    GSHARD_RELU_SMALL,
+    DSMOE_16B_CAP,
     workloads.DSMOE_2B.with_tokens(700),
     workloads.DSMOE_16B.with_tokens(333),
     workloads.GSHARD_NOISY.with_tokens(300),
     workloads.DSMOE_145B.with_tokens(150),
     workloads.DSMOE_145B_DECODE,
 ]
-FULL = [workloads.DSMOE_2B, workloads.DSMOE_16B, workloads.GSHARD_NOISY, workloads.DSMOE_145B]
+FULL = [workloads.DSMOE_2B, workloads.DSMOE_16B, workloads.GSHARD_NOISY, workloads.DSMOE_145B,
+        workloads.GSHARD_RELU_CAP]
 
 _cache = {}
 
@@ -107,11 +119,21 @@ def check_routing(w, r, ids, gates):
 def test_route(w, cuda_lib):
     inp = get_inputs(w, with_experts=False)
     cfg = binding.config(w)
-    ids, g, logits = binding.route(cfg, dev(inp["x"]), dev(inp["W_g"]), dev(inp["W_noise"]),
-                                   dev(inp["eps"]), dev(inp["bias"]), want_logits=True)
+    ids, g, logits, stats = binding.route(cfg, dev(inp["x"]), dev(inp["W_g"]), dev(inp["W_noise"]),
+                                          dev(inp["eps"]), dev(inp["bias"]), want_logits=True,
+                                          want_stats=True)
     r = oracle_route(w, inp)
-    check_routing(w, r, ids, g)
+    ok = check_routing(w, r, ids, g)
     np.testing.assert_allclose(logits.cpu().numpy(), r["logits"], rtol=0, atol=2e-5)
+    # router statistics: per-token logsumexp, per-expert sums of s and of the gates
+    np.testing.assert_allclose(stats["lse"].cpu().numpy(), O.logsumexp(r["logits"]), rtol=0, atol=4e-5)
+    psum = O.prob_column_sums(r["logits"])
+    np.testing.assert_allclose(stats["prob_sum"].cpu().numpy(), psum, rtol=2e-4, atol=1e-3)
+    imp = O.importance(O.dense_gates(r["ids"], r["gates"], w.n_routed))
+    near = r["gates"][~ok].sum()    # tokens under the margin may pick a different (near-equal) expert
+    gsum = stats["gate_sum"].cpu().numpy()
+    assert np.abs(gsum - imp).max() <= 2e-4 * np.abs(imp).max() + 1e-3 + 2 * near
+    assert O.router_z_loss(r["logits"]) == pytest.approx(float(np.mean(stats["lse"].cpu().numpy().astype(np.float64) ** 2)), rel=2e-5)
     ids2, g2 = binding.route(cfg, dev(inp["x"]), dev(inp["W_g"]), dev(inp["W_noise"]),
                              dev(inp["eps"]), dev(inp["bias"]))
     assert torch.equal(ids, ids2) and torch.equal(g, g2), "routing is not deterministic"
@@ -148,6 +170,47 @@ def test_permute_bit_exact(T, E, k, skew, cuda_lib):
     assert st == 0
 
 
+@pytest.mark.parametrize("T,E,k,cap", [(1000, 63, 7, 60), (4097, 128, 12, 300), (300, 16, 2, 1), (2000, 64, 6, 5000)])
+def test_permute_capacity_bit_exact(T, E, k, cap, cuda_lib):
+    """Expert capacity: the first `cap` assignments of each expert (ascending
+    t*k + j) are grouped, the rest get dest = -1 and no row."""
+    d = 128
+    w = workloads.Workload("perm_cap", T=T, d=d, n_routed=E, n_shared=0, top_k=k, d_ff=64, capacity=cap)
+    cfg = binding.config(w)
+    ids = inputs.random_topk_ids(T, E, k, seed=T + cap, skew="hot")
+    x = torch.randn(T, d).to(torch.bfloat16)
+    out = binding.permute(cfg, x.to(DEV), ids.to(DEV))
+    ref = O.dispatch(ids.numpy(), E, capacity=cap)
+    n = int(ref["offsets"][-1])
+    assert (out["counts"].cpu().numpy() == ref["counts"]).all()
+    assert (out["offsets"].cpu().numpy() == ref["offsets"]).all()
+    assert (out["dest"].cpu().numpy() == ref["dest"]).all()
+    assert (out["perm_src"].cpu().numpy()[:n] == ref["perm_src"]).all()
+    assert torch.equal(out["x_perm"].cpu()[:n], x[torch.from_numpy(ref["perm_src"] // k)])
+    st, _ = binding.device_status()
+    assert st == 0
+
+
+def test_stages_with_capacity_match_oracle(cuda_lib):
+    """permute (with capacity) -> expert_ffn -> combine against the oracle's
+    dispatch -> expert_rows -> combine on the same routing."""
+    w = DSMOE_16B_CAP
+    inp = get_inputs(w)
+    cfg = binding.config(w)
+    ids = inputs.random_topk_ids(w.T, w.n_routed, w.top_k, seed=29, skew="hot")
+    gates = inputs.random_gates(w.T, w.top_k, seed=30)
+    g = {k: dev(v) for k, v in inp.items()}
+    p = binding.permute(cfg, g["x"], ids.to(DEV))
+    rows = binding.expert_ffn(cfg, g["x"], p["x_perm"], p["offsets"], g["W1"], g["W3"], g["W2"])
+    y = binding.combine(cfg, rows, p["dest"], gates.to(DEV))
+    dsp = O.dispatch(ids.numpy(), w.n_routed, capacity=w.capacity)
+    assert (dsp["dest"] < 0).any(), "the capacity should drop assignments in this case"
+    ref_rows = O.expert_rows(inp["x"], inp["W1"], inp["W3"], inp["W2"], w.n_shared, dsp["perm_src"],
+                             dsp["offsets"], w.top_k)
+    ref = O.combine(ref_rows, dsp["dest"], gates.numpy(), w.n_shared, w.T)
+    check_close(y.float().cpu().numpy(), ref, False, "capacity stages")
+
+
 def test_permute_flags_out_of_range_ids(cuda_lib):
     w = workloads.Workload("perm_bad", T=64, d=64, n_routed=8, n_shared=0, top_k=2, d_ff=64)
     cfg = binding.config(w)
@@ -180,7 +243,7 @@ def test_expert_ffn(w, cuda_lib):
                              torch.from_numpy(dsp["offsets"].astype(np.int32)).to(DEV),
                              dev(inp["W1"]), dev(inp["W3"]), dev(inp["W2"]))
     ref = O.expert_rows(inp["x"], inp["W1"], inp["W3"], inp["W2"], w.n_shared, dsp["perm_src"],
-                        dsp["offsets"], w.top_k)
+                        dsp["offsets"], w.top_k, act=w.act)
     check_close(out.cpu().numpy(), ref, w.fp32, "expert rows")
     assert binding.device_status()[0] == 0
 
@@ -228,14 +291,26 @@ def forward_case(w, sample):
     ok = check_routing(w, r, ids, gw)
     ids_h = ids.cpu().numpy()
     recount = np.bincount(ids_h.reshape(-1), minlength=w.n_routed)
+    if w.capacity:
+        recount = np.minimum(recount, w.capacity)
     assert (counts.cpu().numpy() == recount).all()
     ref_counts = np.bincount(r["ids"].reshape(-1), minlength=w.n_routed)
+    if w.capacity:
+        ref_counts = np.minimum(ref_counts, w.capacity)
     assert np.abs(recount - ref_counts).sum() <= 2 * w.top_k * int((~ok).sum())
     rng = np.random.default_rng(w.seed)
     toks = np.arange(w.T) if sample is None or sample >= w.T else np.sort(rng.choice(w.T, sample, replace=False))
     toks = toks[ok[toks]]
+    keep = None
+    if w.capacity:
+        # a token's capacity decisions depend on the routing of the tokens before
+        # it: compare only tokens before the first one under the margin
+        first_near = int(np.argmin(ok)) if not ok.all() else w.T
+        toks = toks[toks < first_near]
+        keep = O.capacity_keep(r["ids"], w.n_routed, w.capacity)
+        assert toks.size > 0
     ref = O.moe_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], w.n_shared, r["ids"], r["gates"],
-                        tokens=toks)
+                        tokens=toks, act=w.act, keep=keep)
     got = y.float().cpu().numpy()[toks]
     return check_close(got, ref, w.fp32, f"{w.name} y")
 

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.moe_version() >> 16 == 1
+    assert lib.moe_version() >> 16 == 2
     for s in range(8):
         assert lib.moe_status_string(s).startswith(b"MOE_")
     assert b"unknown" in lib.moe_status_string(99)
@@ -62,7 +62,8 @@ def cfg_of(**kw):
 
 @pytest.mark.parametrize("bad", [
     dict(top_k=17), dict(top_k=0), dict(d=0), dict(T=-1), dict(n_routed=0), dict(gate=2),
-    dict(act_dtype=5), dict(renormalize=2), dict(gate=1, renormalize=0),
+    dict(act_dtype=5), dict(renormalize=2), dict(gate=1, renormalize=0), dict(capacity=-1),
+    dict(expert_act=2),
 ])
 def test_invalid_configs_rejected(lib, bad):
     c = cfg_of(**bad)
@@ -74,14 +75,14 @@ def test_invalid_configs_rejected(lib, bad):
                                  dict(gate=1, renormalize=1, n_routed=129), dict(top_k=33, n_routed=64)])
 def test_unsupported_configs(lib, bad):
     c = cfg_of(**bad)
-    st = lib.moe_route(ctypes.byref(c), *([None] * 8), None, 0, None)
+    st = lib.moe_route(ctypes.byref(c), *([None] * 9), None, 0, None)
     assert st == 2   # MOE_ERR_UNSUPPORTED
 
 
 def test_null_pointers_and_workspace_checked_before_launch(lib):
     c = cfg_of()
     assert fwd_nulls(lib, None) == 1
-    assert lib.moe_route(ctypes.byref(c), *([None] * 8), None, 0, None) == 1
+    assert lib.moe_route(ctypes.byref(c), *([None] * 9), None, 0, None) == 1
     # a too-small workspace is reported before anything touches the device
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
     st = lib.moe_forward(ctypes.byref(c), fake, fake, None, None, None, fake, fake, fake, fake, 16,
