@@ -36,12 +36,19 @@ GSHARD_RELU_SMALL = workloads.Workload("gshard_relu_cap40_T300", T=300, d=512, n
 DSMOE_16B_CAP = workloads.DSMOE_16B.with_tokens(333, "dsmoe16b_cap28_T333")
 DSMOE_16B_CAP = workloads.replace(DSMOE_16B_CAP, capacity=28)
 TINY_RELU = workloads.replace(workloads.TINY_FP32, name="tiny_fp32_relu_T256", act="relu", seed=23)
+# ragged in every dimension: T not a multiple of 128 (or 32), d and I not
+# multiples of 64 (partial k-blocks, partial n-tiles, clipped H stores), E odd
+RAGGED = workloads.Workload("ragged_T129_d520_I200_E23", T=129, d=520, n_routed=23, n_shared=1, top_k=5,
+                            d_ff=200, seed=31)
+RAGGED_BIG = workloads.replace(RAGGED, name="ragged_T4999_d520_I200_E23", T=4999, seed=32)
 SMALL = [
     workloads.TINY_FP32,
     TINY_RELU,
     WIDE_ROUTER,
     GSHARD_RELU_SMALL,
     DSMOE_16B_CAP,
+    RAGGED,
+    RAGGED_BIG,
     workloads.DSMOE_2B.with_tokens(700),
     workloads.DSMOE_16B.with_tokens(333),
     workloads.GSHARD_NOISY.with_tokens(300),
