@@ -194,6 +194,18 @@ def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
     return ms
 
 
+def workload_config(w, world: int, ab: float | None = None) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    cfg = {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
+           "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
+           "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
+           "expert": w.act, "capacity": w.capacity or None,
+           "parallelism": f"replicas x{world}"}
+    if ab is not None:
+        cfg["l2"] = f"inputs larger than L2: {ab / 2**20:.0f} MiB of weights+activations per step"
+    return cfg
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -207,10 +219,10 @@ def run_reference(args, w):
     val = statistics.median(s["value"] for s in timed)
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights)",
-            "config": {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
-                       "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff},
+            "ms_per_step": 1e3 * w.T / val,   # one step = the workload's T tokens at the sampled rate
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; no checkpoint)",
+            "config": workload_config(w, world),
             "cpu_baseline": {**timed[-1], "value": val},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -327,12 +339,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.fp32 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; no checkpoint)",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
-                   "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
-                   "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
-                   "expert": w.act, "capacity": w.capacity or None,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {ab / 2**20:.0f} MiB of weights+activations per step"},
+        "config": workload_config(w, world, ab),
         "tflops": tflops,
         "roofline_fraction_layer": roof_time / (ms_step / 1e3) * world,
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm_tc<SwiGLU> (gate-up)",
