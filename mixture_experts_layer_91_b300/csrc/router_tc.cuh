@@ -24,11 +24,10 @@
 //   warp 0      TMA producer: x [128 x 64] and the three W planes [NP x 64]
 //               per k-block into a multi-stage ring;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               M=128 K=16 with the three planes stacked as one B operand
-//               (N = 3 NP; at NP = 128 one N = 256 MMA for hi | mid and one
-//               N = 128 MMA adding lo onto mid, whose products are 2^-9
-//               smaller, so sharing their accumulator costs nothing),
-//               double-buffered over chunks;
+//               M=128 K=16: one N = 2 NP MMA over the stacked hi | mid planes
+//               and one N = NP MMA adding lo onto mid (lo's products are 2^-9
+//               of mid's, so sharing their accumulator costs nothing), into
+//               2-4 accumulator buffers rotated over chunks;
 //   warps 2-5   clear the tile's rows of the fp32 combine accumulator (forward
 //               path), then drain each chunk (warp w reads the TMEM lanes of
 //               quarter w % 4: one token per thread) into NP fp32 registers,
@@ -53,14 +52,15 @@ struct RtcShape {
   static constexpr uint32_t B_BYTES = NP * 64 * 2;    // one W plane, NP columns x 64 k
   static constexpr uint32_t STAGE_BYTES = A_BYTES + 3 * B_BYTES;
   static constexpr int LS = NP + 1;                   // row stride of the per-token logits rows
-  // One accumulator buffer holds hi | mid | lo side by side (3 NP columns)
-  // when 3 NP <= 256, so one MMA of N = 3 NP covers all three planes; at
-  // NP = 128 it holds hi | (mid + lo) (256 columns): one MMA of N = 256 for
-  // hi | mid and one of N = 128 adding lo onto the mid columns.
-  static constexpr bool STACK3 = 3 * NP <= 256;
-  static constexpr uint32_t BUF_COLS = NP == 32 ? 128 : 256;   // column stride of the 2 buffers
-  static constexpr uint32_t TMEM_COLS = 2 * BUF_COLS;
-  static constexpr size_t smem_bytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 128;
+  // One accumulator buffer holds hi | (mid + lo) side by side (2 NP columns):
+  // one MMA of N = 2 NP for the stacked hi | mid planes, one of N = NP adding
+  // lo onto the mid columns (lo's products are 2^-9 of mid's, so sharing their
+  // accumulator costs nothing). Up to four buffers let the MMAs run three
+  // chunks ahead of the drains.
+  static constexpr uint32_t BUF_COLS = 2 * NP;
+  static constexpr int NBUF = 512 / BUF_COLS < 4 ? 512 / BUF_COLS : 4;
+  static constexpr uint32_t TMEM_COLS = NBUF * BUF_COLS;   // 256 or 512: a power of two
+  static constexpr size_t smem_bytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256;
   static_assert(128ull * LS * 4 <= static_cast<size_t>(STAGES) * STAGE_BYTES, "epilogue rows");
 };
 
@@ -130,11 +130,11 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   uint8_t* gBar = gbase + S::STAGES * S::STAGE_BYTES;
   const uint32_t bar_full = sBar;                    // [STAGES]
   const uint32_t bar_empty = sBar + 8 * S::STAGES;   // [STAGES]
-  const uint32_t bar_tfull = sBar + 16 * S::STAGES;  // [2]
-  const uint32_t bar_tempty = bar_tfull + 16;        // [2]
-  const uint32_t bar_done = bar_tempty + 16;         // every MMA issued has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 16 * S::STAGES + 40);
-  volatile int* abort = reinterpret_cast<volatile int*>(gBar + 16 * S::STAGES + 44);
+  const uint32_t bar_tfull = sBar + 16 * S::STAGES;      // [NBUF]
+  const uint32_t bar_tempty = bar_tfull + 8 * S::NBUF;   // [NBUF]
+  const uint32_t bar_done = bar_tempty + 8 * S::NBUF;    // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 16 * S::STAGES + 16 * S::NBUF + 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(gBar + 16 * S::STAGES + 16 * S::NBUF + 12);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 128;
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < S::NBUF; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, 4);
     }
@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
       bool ok = true;
       int32_t kb = 0;
       for (int32_t ch = 0; ch < nchunk && ok; ++ch) {
-        const uint32_t b = ch & 1;
-        if (!mbar_wait(bar_tempty + 8 * b, ((ch >> 1) & 1u) ^ 1u, abort)) { ok = false; break; }
+        const uint32_t b = ch % S::NBUF;
+        if (!mbar_wait(bar_tempty + 8 * b, ((ch / S::NBUF) & 1u) ^ 1u, abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t acc = tmem_base + b * S::BUF_COLS;
         for (int32_t j = 0; j < kRtcChunk && kb < nk; ++j, ++kb) {
@@ -211,20 +211,14 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
           tc_fence_after();
           const uint32_t sa = base + s * S::STAGE_BYTES;
           const uint64_t ad = sdesc_kmajor_sw128(sa);
-          const uint64_t bd = sdesc_kmajor_sw128(sa + S::A_BYTES);   // hi, mid, lo rows stacked
-          if constexpr (S::STACK3) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, 3 * NP);
+          const uint64_t bd = sdesc_kmajor_sw128(sa + S::A_BYTES);   // hi, mid rows stacked
+          const uint64_t bl = sdesc_kmajor_sw128(sa + S::A_BYTES + 2 * S::B_BYTES);
+          constexpr uint32_t idesc2 = idesc_bf16_f32(128, 2 * NP);
+          constexpr uint32_t idesc1 = idesc_bf16_f32(128, NP);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc, (j | kk) != 0);
-          } else {
-            constexpr uint32_t idesc2 = idesc_bf16_f32(128, 2 * NP);
-            constexpr uint32_t idesc1 = idesc_bf16_f32(128, NP);
-            const uint64_t bl = sdesc_kmajor_sw128(sa + S::A_BYTES + 2 * S::B_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc2, (j | kk) != 0);
-              tc_mma_bf16(acc + NP, ad + 2 * kk, bl + 2 * kk, idesc1, 1);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc2, (j | kk) != 0);
+            tc_mma_bf16(acc + NP, ad + 2 * kk, bl + 2 * kk, idesc1, 1);
           }
           tc_commit(bar_empty + 8 * s);
         }
@@ -258,28 +252,19 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   bool ok = true;
   const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   for (int32_t ch = 0; ch < nchunk; ++ch) {
-    const uint32_t b = ch & 1;
-    ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_tfull + 8 * b, (ch >> 1) & 1u, abort));
+    const uint32_t b = ch % S::NBUF;
+    ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_tfull + 8 * b, (ch / S::NBUF) & 1u, abort));
     if (!ok) break;
     tc_fence_after();
 #pragma unroll
     for (int cc = 0; cc < NP / 32; ++cc) {
       const uint32_t col = tl + b * S::BUF_COLS + cc * 32;
-      uint32_t hi[32], mid[32];
+      uint32_t hi[32], ml[32];
       tmem_ld_32x32b_x32(col, hi);
-      tmem_ld_32x32b_x32(col + NP, mid);
-      if constexpr (S::STACK3) {
-        uint32_t lo[32];
-        tmem_ld_32x32b_x32(col + 2 * NP, lo);
-        tmem_ld_wait();
+      tmem_ld_32x32b_x32(col + NP, ml);
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          acc[cc * 32 + j] += __uint_as_float(hi[j]) + (__uint_as_float(mid[j]) + __uint_as_float(lo[j]));
-      } else {
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(mid[j]);
-      }
+      for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(ml[j]);
     }
     tc_fence_before();
     __syncwarp();
