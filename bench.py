@@ -58,6 +58,30 @@ def dist_env():
     return world, rank, local
 
 
+def replica_inputs(w, rank: int) -> dict:
+    """Replica `rank` of the data-parallel run: the same layer (weights drawn
+    from the workload's seed) on its own batch of tokens (weak scaling: the
+    layer's tokens are independent, so replicas never exchange data)."""
+    inp = inputs.make_inputs(w)
+    if rank > 0:
+        inp.update(inputs.make_tokens(w, rank))
+    return inp
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The slowest rank's time (all_reduce MAX; identity on one rank)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def kernel_flops(w, kept: int) -> dict:
     """Algorithmic FLOPs per launch of each kernel: `kept` routed rows (T*k
     when dropless, fewer under an expert capacity) + K_s*T shared rows; each
@@ -186,12 +210,7 @@ def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
     e_start.record(stream)
     e_end = run(n)
     barrier()
-    ms = e_start.elapsed_time(e_end) / n
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = tt.item()
-    return ms
+    return max_over_ranks(e_start.elapsed_time(e_end) / n, world, dev)
 
 
 def workload_config(w, world: int, ab: float | None = None) -> dict:
@@ -256,7 +275,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    inp = inputs.make_inputs(w)
+    inp = replica_inputs(w, rank)
     layer = binding.MoELayer(w, inp, device=dev)
     x = inp["x"].to(dev)
     eps = inp["eps"].to(dev) if inp["eps"] is not None else None
@@ -287,11 +306,7 @@ def main():
     st, raw = binding.device_status()
     if st != 0:
         raise RuntimeError(f"device fault flag {raw} after the timed region")
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = tt.item()
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
     stage_names = ["router", "dispatch", "gate_up", "down", "cast"]
     stage_ms = {n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_ev)
@@ -325,7 +340,7 @@ def main():
     src = os.path.join(ROOT, "mixture_experts_layer_91_b300", "csrc", "gemm_tc.cuh")
     tr = ncu_traffic(src)
     flops = kf["router"] + kf["gate_up"] + kf["down"]
-    tokens_per_s = world * w.T / (ms_step / 1e3)
+    tokens_per_s = job_tokens_per_s(world, w.T, ms_step)
     tflops = world * flops / (ms_step / 1e3) / 1e12
     ab = algorithmic_bytes(w, touched)
     roof_time = max(flops / (pk["bf16_tflops"] * 1e12), ab / (pk["hbm_gbs"] * 1e9))
@@ -353,7 +368,7 @@ def main():
                            "down": kf["down"] / (stage_ms["down"] / 1e3) / 1e12,
                            "router": kf["router"] / (stage_ms["router"] / 1e3) / 1e12},
         "e2e": None if ms_e2e is None else {
-            "value": world * w.T / (ms_e2e / 1e3), "unit": "tokens/s",
+            "value": job_tokens_per_s(world, w.T, ms_e2e), "unit": "tokens/s",
             "h2d_bytes_per_step": x_host_bytes + eps_bytes, "d2h_bytes_per_step": y_bytes},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

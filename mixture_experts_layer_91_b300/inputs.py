@@ -56,6 +56,18 @@ def make_inputs(w: Workload, *, with_experts: bool = True) -> dict:
     return out
 
 
+def make_tokens(w: Workload, replica: int) -> dict:
+    """The token-side inputs (x, and eps for the noisy gate) of another batch
+    of the same layer: replica r > 0 of a data-parallel run draws its own
+    batch from generator seed + 1000 r (replica 0 uses make_inputs' x)."""
+    g = _gen(w.seed + 1000 * replica)
+    act = torch.float32 if w.fp32 else torch.bfloat16
+    out = {"x": torch.randn(w.T, w.d, generator=g).to(act), "eps": None}
+    if w.noisy:
+        out["eps"] = torch.randn(w.T, w.n_routed, generator=g)
+    return out
+
+
 def _randn_chunked(shape, g, dtype) -> torch.Tensor:
     """N(0, WEIGHT_STD^2) drawn expert by expert (bounded fp32 temporaries)."""
     out = torch.empty(shape, dtype=dtype)
