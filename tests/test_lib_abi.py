@@ -114,3 +114,31 @@ def test_zero_tokens_is_a_no_op(lib):
     assert lib.moe_expert_ffn(ctypes.byref(c), None, None, None, None, None, None, None, 0, None,
                               None) == 0
     assert lib.moe_combine(ctypes.byref(c), None, None, None, None, None) == 0
+
+
+def test_route_workspace_size_matches_the_router_choice(lib):
+    """The tensor-core router (bf16, <= 128 router columns, T >= 4096) needs the
+    three bf16 planes of [W_g | W_noise]: 3 x NP x d x 2 bytes, NP the columns
+    rounded up to 32 / 64 / 128; the CUDA-core router needs nothing."""
+    big = dict(T=4096, d=256, act_dtype=1)
+    for n_routed, gate, renorm, np_ in [(16, 0, 0, 32), (64, 0, 0, 64), (63, 0, 0, 64), (128, 0, 0, 128),
+                                        (16, 1, 1, 32), (64, 1, 1, 128)]:
+        c = cfg_of(**big, n_routed=n_routed, gate=gate, renormalize=renorm)
+        assert lib.moe_route_workspace_size(ctypes.byref(c)) == 3 * np_ * 256 * 2
+    for kw in (dict(T=4095), dict(act_dtype=0), dict(n_routed=129), dict(n_routed=65, gate=1, renormalize=1)):
+        c = cfg_of(**{**big, "n_routed": 64, **kw})
+        assert lib.moe_route_workspace_size(ctypes.byref(c)) == 0
+    # a workspace short of the planes is refused before any launch
+    c = cfg_of(**big, n_routed=64)
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.moe_route(ctypes.byref(c), fake, fake, None, None, None, fake, fake, None, None, fake, 16, None)
+    assert st == 3   # MOE_ERR_WORKSPACE
+
+
+def test_relu_experts_take_no_w3_but_swiglu_needs_it(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    for act, want in ((0, 1), (1, 3)):   # SwiGLU: null W3 is an error; ReLU: passes on to the workspace check
+        c = cfg_of(expert_act=act, act_dtype=1)
+        st = lib.moe_forward(ctypes.byref(c), fake, fake, None, None, None, fake, None, fake, fake, 16,
+                             fake, None, None, None, None)
+        assert st == want
