@@ -31,9 +31,9 @@
 //   warps 2-5   clear the tile's rows of the fp32 combine accumulator (forward
 //               path), then drain each chunk (warp w reads the TMEM lanes of
 //               quarter w % 4: one token per thread) into NP fp32 registers,
-//               and finally compute that token's softmax and top-k in
-//               registers (eight interleaved arg-max chains per round, ties to
-//               the lower expert index).
+//               and finally compute that token's softmax and top-k over its
+//               logits row in shared memory (eight interleaved arg-max chains
+//               per round, ties to the lower expert index).
 #pragma once
 
 #include "common.cuh"
@@ -61,7 +61,7 @@ struct RtcShape {
   static constexpr int NBUF = 512 / BUF_COLS < 4 ? 512 / BUF_COLS : 4;
   static constexpr uint32_t TMEM_COLS = NBUF * BUF_COLS;   // 256 or 512: a power of two
   static constexpr size_t smem_bytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256;
-  static_assert(128ull * LS * 4 <= static_cast<size_t>(STAGES) * STAGE_BYTES, "epilogue rows");
+  static_assert(2ull * 128 * LS * 4 <= static_cast<size_t>(STAGES) * STAGE_BYTES, "epilogue rows");
 };
 
 // The three bf16 planes of W = [W_g | W_noise] ([d, cols] fp32, row-major),
@@ -279,54 +279,67 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   const bool valid = t < p.T;
   const int E = p.E;
 
-  // logits row in shared memory (the operand ring is idle now: every load
-  // landed and every MMA that read it completed) for the lookups of the picks
-  float* Lrow = reinterpret_cast<float*>(gbase) + row * S::LS;
+  // The per-token work below runs once per CTA, so it is written as short
+  // loops over shared-memory rows rather than unrolled register code: the
+  // unrolled form was bound by instruction fetch (each SM meets it cold).
+  // Rows live in the operand ring, idle now (every load landed and every MMA
+  // that read it completed); stride LS = NP + 1 keeps a warp's 32 rows on 32
+  // banks.
+  float* Lrow = reinterpret_cast<float*>(gbase) + row * S::LS;           // logits
+  float* Krow = reinterpret_cast<float*>(gbase) + (128 + row) * S::LS;   // selection keys
 #pragma unroll
   for (int c = 0; c < NP; ++c) Lrow[c] = acc[c];
   if (p.logits_out != nullptr && valid)
     for (int c = 0; c < E; ++c) p.logits_out[t * E + c] = Lrow[c];
 
+  // softmax over the E gate logits: max, then the sum of exponentials, each
+  // in four interleaved partial chains (element c feeds chain c % 4)
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  for (int c = 0; c < E; c += 4) {
 #pragma unroll
-  for (int c = 0; c < NP; ++c)
-    if (c < E) mx[c & 3] = fmaxf(mx[c & 3], acc[c]);
+    for (int j = 0; j < 4; ++j)
+      if (c + j < E) mx[j] = fmaxf(mx[j], Lrow[c + j]);
+  }
   const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   float sm[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < E; c += 4) {
 #pragma unroll
-  for (int c = 0; c < NP; ++c)
-    if (c < E) sm[c & 3] += expf(acc[c] - m);
+    for (int j = 0; j < 4; ++j)
+      if (c + j < E) sm[j] += expf(Lrow[c + j] - m);
+  }
   const float ssum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
   const float inv = 1.0f / ssum;
   if (p.lse != nullptr && valid) p.lse[t] = m + logf(ssum);
   if (p.prob_sum != nullptr) {
     // sum of s over this warp's 32 tokens per expert, then one atomic per warp
+#pragma unroll 4
+    for (int c = 0; c < E; ++c) {
+      float v = valid ? expf(Lrow[c] - m) * inv : 0.f;
 #pragma unroll
-    for (int c = 0; c < NP; ++c) {
-      if (c < E) {   // uniform across the warp
-        float v = valid ? expf(acc[c] - m) * inv : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) atomicAdd(p.prob_sum + c, v);
-      }
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) atomicAdd(p.prob_sum + c, v);
     }
   }
   if (!valid) return;
 
-  // selection keys, in place; NaN = not selectable
+  // selection keys; NaN = not selectable (also the padding up to a multiple of 8)
   const float nan = __int_as_float(0x7fffffff);
-#pragma unroll
-  for (int c = 0; c < NP; ++c) {
+  const int E8 = (E + 7) & ~7;   // <= NP
+  for (int c = 0; c < E8; ++c) {
     float key = nan;
     if (c < E) {
-      if (p.noisy) key = acc[c] + p.eps[t * E + c] * softplus_f(Lrow[c + E]);
-      else if (p.bias != nullptr) key = expf(acc[c] - m) * inv + __ldg(p.bias + c);
-      else key = acc[c];   // Softmax is increasing: the order of s is the order of the logits
+      const float l = Lrow[c];
+      if (p.noisy) key = l + p.eps[t * E + c] * softplus_f(Lrow[c + E]);
+      else if (p.bias != nullptr) key = expf(l - m) * inv + __ldg(p.bias + c);
+      else key = l;   // Softmax is increasing: the order of s is the order of the logits
       if (key != key) key = -INFINITY;   // a NaN key ranks last, ids stay valid
     }
-    acc[c] = key;
+    Krow[c] = key;
   }
 
+  // k rounds of arg-max: eight chains (chain j scans c = j, j + 8, ... in
+  // increasing order), merged with ties to the lower index; the pick is then
+  // marked taken
   float sel_sum = 0.f, key0 = 0.f;
   for (int r = 0; r < p.k; ++r) {
     float kb8[8];
@@ -336,16 +349,20 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
       kb8[j] = nan;
       ib8[j] = -1;
     }
+#pragma unroll 2
+    for (int c = 0; c < E8; c += 8) {
 #pragma unroll
-    for (int c = 0; c < NP; ++c) argmax_step(acc[c], c, kb8[c & 7], ib8[c & 7]);
+      for (int j = 0; j < 8; ++j) argmax_step(Krow[c + j], c + j, kb8[j], ib8[j]);
+    }
 #pragma unroll
     for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
       for (int j = 0; j < w; ++j) argmax_merge(kb8[j + w], ib8[j + w], kb8[j], ib8[j]);
     const float kb = kb8[0];
-    const int bi = ib8[0];   // k <= E: a selectable entry remains every round
-#pragma unroll
-    for (int c = 0; c < NP; ++c) acc[c] = (c == bi) ? nan : acc[c];
+    // k <= E and no key below E is NaN, so a selectable entry remains every
+    // round; the clamp only keeps the row accesses in bounds regardless
+    const int bi = max(ib8[0], 0);
+    Krow[bi] = nan;
     float v;
     if (p.noisy) {
       if (r == 0) key0 = kb;

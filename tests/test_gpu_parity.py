@@ -146,8 +146,25 @@ def test_route(w, cuda_lib):
     assert torch.equal(ids, ids2) and torch.equal(g, g2), "routing is not deterministic"
 
 
-def test_route_ties_pick_lowest_index(cuda_lib):
-    w = workloads.DSMOE_16B.with_tokens(70)
+# Router-only cases for the tensor-core router (bf16, T >= 4096): expert counts
+# that are not a multiple of 8 and a reduction width with a partial last
+# k-block and an odd number of tensor-memory drains.
+TC_ROUTE_NOISY_ODD = workloads.Workload("tc_route_noisy_e63_T4100", T=4100, d=520, n_routed=63, n_shared=0,
+                                        top_k=7, d_ff=64, renormalize=True, noisy=True, seed=31)
+TC_ROUTE_BIAS_ODD = workloads.Workload("tc_route_bias_e20_T4133", T=4133, d=1000, n_routed=20, n_shared=0,
+                                       top_k=3, d_ff=64, bias=True, seed=32)
+
+
+@pytest.mark.parametrize("w", [TC_ROUTE_NOISY_ODD, TC_ROUTE_BIAS_ODD], ids=lambda w: w.name)
+def test_route_tensor_core_odd_shapes(w, cuda_lib):
+    test_route(w, cuda_lib)
+
+
+@pytest.mark.parametrize("T,E,k", [(70, 64, 6), (4101, 64, 6), (4101, 63, 7), (4101, 20, 3), (4101, 128, 12)])
+def test_route_ties_pick_lowest_index(T, E, k, cuda_lib):
+    """All logits equal (W_g = 0): the picks are experts 0..k-1 in order with
+    gates 1/E, on the CUDA-core router (T < 4096) and the tensor-core one."""
+    w = workloads.Workload("ties", T=T, d=256, n_routed=E, n_shared=0, top_k=k, d_ff=64)
     cfg = binding.config(w)
     x = torch.randn(w.T, w.d, device=DEV).to(torch.bfloat16)
     ids, g = binding.route(cfg, x, torch.zeros(w.d, w.n_routed, device=DEV))
