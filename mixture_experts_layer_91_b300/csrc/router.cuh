@@ -18,9 +18,10 @@
 // double-buffered: W through cp.async, x through registers (widened to fp32 on
 // the way into shared memory). The per-warp partial tiles are summed in shared
 // memory in a fixed order. When T is small a thread-block cluster of CS CTAs
-// also splits the k-chunks, and the leader CTA adds the other CTAs' tiles
-// through distributed shared memory. The leader then computes, one warp per
-// token, the softmax and a k-round warp arg-max (ties to the lower index).
+// also splits the k-chunks; each CTA of the cluster then owns BT / CS of the
+// tokens and adds their partial rows from every CTA's tile through
+// distributed shared memory (ranks in order). Per token, one warp computes the
+// softmax and a k-round warp arg-max (ties to the lower index).
 #pragma once
 
 #include "common.cuh"
@@ -345,28 +346,38 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
     part[tok * S::LS + col] = s;
   }
   __syncthreads();
+  // Tokens this CTA finishes: all of the tile, or with a cluster its rank's
+  // share (BT / csize consecutive tokens).
+  int tok_begin = 0, tok_end = S::BT;
   if (csize > 1) {
-    // the leader adds the other CTAs' tiles (ranks in order: fixed summation order)
-    cluster_sync_all();
-    if (crank == 0) {
-      const uint32_t local = smem_addr(part);
-      for (int idx = tid; idx < S::BT * EPAD; idx += kRouterThreads) {
-        const int tok = idx / EPAD, col = idx % EPAD;
-        const uint32_t off = (tok * S::LS + col) * 4;
-        float s = part[tok * S::LS + col];
-        for (uint32_t r = 1; r < csize; ++r) s += ld_shared_cluster_f32(mapa_shared(local + off, r));
-        part[tok * S::LS + col] = s;
-      }
+    // Each CTA adds the cluster's partial rows of its own tokens, ranks in
+    // order (a fixed summation order), in place: the rows a CTA rewrites are
+    // read by no other CTA.
+    const int share = S::BT / static_cast<int>(csize);
+    tok_begin = static_cast<int>(crank) * share;
+    tok_end = tok_begin + share;
+    cluster_sync_all();   // every CTA's partial tile is complete
+    const uint32_t local = smem_addr(part);
+    for (int idx = tid; idx < share * EPAD; idx += kRouterThreads) {
+      const int tok = tok_begin + idx / EPAD, col = idx % EPAD;
+      const uint32_t off = (tok * S::LS + col) * 4;
+      float v[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        v[r] = r < static_cast<int>(csize) ? ld_shared_cluster_f32(mapa_shared(local + off, r)) : 0.f;
+      float s = v[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r)
+        if (r < static_cast<int>(csize)) s += v[r];
+      part[tok * S::LS + col] = s;
     }
-    cluster_sync_all();   // the other CTAs stay resident until the leader has read them
-    if (crank != 0) return;
-    __syncthreads();
+    cluster_sync_all();   // no CTA leaves while another still reads its tile
   }
 
   // per-token softmax + top-k: one warp per token
   constexpr int PER_LANE = EPAD / 32;
   const float* L = part;
-  for (int tok = warp; tok < S::BT; tok += kRouterWarps) {
+  for (int tok = tok_begin + warp; tok < tok_end; tok += kRouterWarps) {
     const int64_t t = t0 + tok;
     if (t >= p.T) break;
     const float* Lr = L + tok * S::LS;
