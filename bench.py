@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step is one whole layer forward (router, dispatch, gate-up GEMM with
-SwiGLU, down GEMM with the gate-weighted scatter-add, cast) over one batch of
+SwiGLU, down GEMM, gate-weighted combine) over one batch of
 T synthetic tokens, inputs resident in HBM. Default workload: the
 DeepSeekMoE-16B-shaped layer at T = 16384 tokens. With N > 1 (torchrun) every
 rank runs an independent replica on its own GPU (the layer's tokens are
@@ -355,7 +355,7 @@ def main():
         raise RuntimeError(f"device fault flag {raw} after the timed region")
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
-    stage_names = ["router", "dispatch", "gate_up", "down", "cast"]
+    stage_names = ["router", "dispatch", "gate_up", "down", "combine"]
     stage_ms = {n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_ev)
                 for j, n in enumerate(stage_names)}
 
@@ -388,7 +388,7 @@ def main():
     tflops = world * flops / (ms_step / 1e3) / 1e12
     ab = algorithmic_bytes(w, touched)
     roof_time = max(flops / (pk["bf16_tflops"] * 1e12), ab / (pk["hbm_gbs"] * 1e9))
-    # bf16: [W split] + router + count + scan + rank + gate-up + down + cast;
+    # bf16: [W split] + router + count + scan + rank + gate-up + down + combine;
     # fp32: router + count + scan + scatter + gate-up + down
     tc_router = (not w.fp32) and (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
     launches_per_step = 6 if w.fp32 else (8 if tc_router else 7)

@@ -249,16 +249,22 @@ size_t moe_workspace_size(const moe_config* cfg);
 
 /*
  * moe_forward -- the whole layer: route, dispatch, grouped SwiGLU experts and
- * the gate-weighted combine, fused as: router -> histogram/scan/plan ->
- * gather -> gate-up GEMM with SiLU*up fused -> down GEMM whose epilogue
- * scatter-adds g * FFN into an fp32 accumulator (shared experts at gate 1)
- * -> cast to y. Arguments as in moe_route / moe_expert_ffn.
+ * the gate-weighted combine ([DSMoE] section 3.2, eq (9)), fused as: router
+ * -> histogram/scan/plan -> gather -> gate-up GEMM with SiLU*up fused ->
+ * down GEMM -> combine. bf16 layers: the down GEMM stores each expert row
+ * FFN_e(u_t) as bf16 (the K_s shared experts summed into one row per token),
+ * and the combine kernel forms y_t = shared row + sum_j g_{t,j} row(t, j) in
+ * fp32, in a fixed order, rounded once to bf16. fp32 layers: the down GEMM
+ * adds g * FFN into y with fp32 atomics. Arguments as in moe_route /
+ * moe_expert_ffn. ([DSMoE]: the DeepSeekMoE paper, Chinese translation on
+ * gitcode.csdn.net.)
  *   y            [T, d]  act_dtype (out)
  *   topk_ids_out [T, k]  int32 or NULL (out) routing decisions
  *   topk_w_out   [T, k]  fp32  or NULL (out) gate values
  *   counts_out   [N_r]   int32 or NULL (out) tokens per routed expert
- * The scatter-add uses fp32 atomics, so the summation order of the k + K_s
- * contributions to a token (not the result's tolerance) varies run to run.
+ * bf16 layers give the same y on every run; in fp32 layers the atomics'
+ * summation order of a token's k + K_s contributions (not the result's
+ * tolerance) varies run to run.
  */
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
                        const float* W_noise, const float* eps, const float* bias,
@@ -277,7 +283,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
  * MOE_PROFILE_EVENTS cudaEvent_t handles (or is NULL, which makes the call
  * identical to moe_forward): [0] before the router, [1] after the router,
  * [2] after dispatch (count, scan+plan, gather), [3] after the gate-up GEMM,
- * [4] after the down GEMM with the scatter-add, [5] after the cast to y.
+ * [4] after the down GEMM, [5] after the combine into y (bf16 layers; for
+ * fp32 layers the down GEMM's scatter-add already formed y).
  */
 moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const float* W_g,
                                 const float* W_noise, const float* eps, const float* bias,

@@ -12,8 +12,10 @@
 //                  per-block rank bases, and the GEMM group plan;
 //   scatter_kernel dest / perm_src and the row gather x -> x_perm (16-byte
 //                  vectors, one warp per assignment).
-// combine_kernel is the gate-weighted sum back to token order (DeepSeekMoE
-// translation, section 3.2, eq (9), without the residual).
+// combine_kernel (fp32 per-row outputs of the stage API) and
+// combine_rows_bf16_kernel (the bf16 forward's rows at padded H rows) are the
+// gate-weighted sum back to token order (DeepSeekMoE translation, section 3.2,
+// eq (9), without the residual).
 #pragma once
 
 #include "common.cuh"
@@ -251,19 +253,68 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// fp32 accumulator -> bf16 output, 8 elements per thread per step.
+// The combine of the bf16 forward ([DSMoE] section 3.2, eq (9)):
+//   y_t = O[t] + sum_j g_{t,j} O[row(t, j)]
+// over the down projection's bf16 rows O [P, d] at padded H rows: row t of
+// the folded shared group (present when K_s > 0) holds the sum of the shared
+// experts for token t; assignment (t, j) of routed expert e = ids[t, j] sits at
+// 128 * mt_start[K_s + e] + (dest[t, j] - a_row[K_s + e]). Assignments an
+// expert's capacity refused (dest = -1) add nothing. fp32 sums in a fixed
+// order (shared row, then j = 0..k-1), rounded once to bf16. One warp per
+// token; lane j < k holds assignment j's row and gate, each lane sums 8
+// columns (one 16-byte vector) per step. k <= 32.
 __global__ void __launch_bounds__(256)
-    cast_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n8) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(src) + 2 * i);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 2 * i + 1);
+    combine_rows_bf16_kernel(const __nv_bfloat16* __restrict__ O, const int32_t* __restrict__ dest,
+                             const int32_t* __restrict__ ids, const float* __restrict__ w,
+                             const int32_t* __restrict__ mt_start, const int32_t* __restrict__ a_row,
+                             int64_t T, int32_t d, int32_t k, int32_t K_s, __nv_bfloat16* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;   // warp-uniform
+  int32_t my_row = -1;
+  float my_g = 0.f;
+  if (lane < k) {
+    const int32_t r = __ldg(dest + t * k + lane);
+    if (r >= 0) {
+      const int32_t g = K_s + __ldg(ids + t * k + lane);
+      my_row = 128 * __ldg(mt_start + g) + (r - __ldg(a_row + g));
+      my_g = __ldg(w + t * k + lane);
+    }
+  }
+  // the column loop is warp-uniform (the shuffles below need every lane)
+  for (int32_t c0 = 0; c0 < d; c0 += 32 * 8) {
+    const int32_t c = c0 + lane * 8;
+    const bool in = c < d;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (K_s > 0 && in) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(O + t * d + c));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __uint_as_float(u[i] << 16);
+        acc[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
+      const float g = __shfl_sync(0xffffffffu, my_g, j);
+      if (row < 0 || !in) continue;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(O + static_cast<int64_t>(row) * d + c));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(g, __uint_as_float(u[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(g, __uint_as_float(u[i] & 0xffff0000u), acc[2 * i + 1]);
+      }
+    }
     uint4 o;
-    o.x = pack_bf16x2(a.x, a.y);
-    o.y = pack_bf16x2(a.z, a.w);
-    o.z = pack_bf16x2(b.x, b.y);
-    o.w = pack_bf16x2(b.z, b.w);
-    reinterpret_cast<uint4*>(dst)[i] = o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    if (in) *reinterpret_cast<uint4*>(y + t * d + c) = o;
   }
 }
 

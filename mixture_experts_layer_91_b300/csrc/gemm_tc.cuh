@@ -55,7 +55,13 @@ constexpr uint32_t kTmemCols = 512;                   // two 256-column fp32 acc
 constexpr uint32_t kStoreBoxBytes = 32 * 32 * 2;       // 32 rows x 32 bf16 columns
 constexpr int kMaxGroups = 512;
 
-enum EpiMode : int { kEpiSwiGLU = 0, kEpiStoreRows = 1, kEpiScatterAdd = 2 };
+// Epilogues: SwiGLU (gate-up: silu(gate) * up, or ReLU, stored as bf16 H);
+// StoreRows (down: fp32 rows in grouped order); ScatterAdd (down: gate-scaled
+// rows added into the fp32 y[token]); StoreBf16 (down: bf16 rows stored at the
+// tile's padded H rows, for a per-token combine kernel).
+enum EpiMode : int { kEpiSwiGLU = 0, kEpiStoreRows = 1, kEpiScatterAdd = 2, kEpiStoreBf16 = 3 };
+
+__host__ __device__ constexpr bool epi_stores_bf16(int mode) { return mode == kEpiSwiGLU || mode == kEpiStoreBf16; }
 
 // Device-side plan of the grouped problem (written by plan_groups()).
 struct GroupPlan {
@@ -88,13 +94,13 @@ struct TcMaps {
   CUtensorMap a1;   // gate-up: x_perm [T*k, d] (routed groups); down: unused
   CUtensorMap b0;   // gate-up: W1 [G*I, d] box 128 rows; down: W2 [G*d, I] box 256 rows
   CUtensorMap b1;   // gate-up: W3 [G*I, d] box 128 rows; down: unused
-  CUtensorMap out;  // gate-up: H [P, I] store box 32 x 32, 64-byte swizzle; down: unused
+  CUtensorMap out;  // store box 32 x 32, 64-byte swizzle: gate-up H [P, I]; down (StoreBf16) O [P, d]
 };
 
 constexpr size_t tc_smem_bytes(int mode) {
   return 1024                                            // alignment slack
          + static_cast<size_t>(kTcStages) * kStageBytes  // operand ring
-         + (mode == kEpiSwiGLU ? kTcEpiWarps * 2 * kStoreBoxBytes : 0)
+         + (epi_stores_bf16(mode) ? kTcEpiWarps * 2 * kStoreBoxBytes : 0)
          + 256;                                          // barriers, TMEM slot, abort flag
 }
 
@@ -147,8 +153,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const uint32_t sA0 = base;                                  // stage s: A at sA0 + s*kStageBytes
   const uint32_t sB0 = base + kTileABytes;                    //          B right after A
-  const uint32_t sStore = base + kTcStages * kStageBytes;     // epilogue staging (gate-up)
-  const uint32_t sBar = sStore + (MODE == kEpiSwiGLU ? kTcEpiWarps * 2 * kStoreBoxBytes : 0);
+  const uint32_t sStore = base + kTcStages * kStageBytes;     // epilogue staging (bf16 stores)
+  const uint32_t sBar = sStore + (epi_stores_bf16(MODE) ? kTcEpiWarps * 2 * kStoreBoxBytes : 0);
   uint8_t* gBar = gbase + (sBar - base);
   // barrier block: full[S] empty[S] tfull[2] tempty[2] drain; then TMEM slot, abort flag
   const uint32_t bar_full = sBar;
@@ -181,8 +187,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (MODE == kEpiSwiGLU) {
       tma_prefetch_desc(&maps.a1);
       tma_prefetch_desc(&maps.b1);
-      tma_prefetch_desc(&maps.out);
     }
+    if (epi_stores_bf16(MODE)) tma_prefetch_desc(&maps.out);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool valid = false;
       int64_t orow = 0;
       float gate = 1.0f;
-      if (MODE != kEpiSwiGLU) {
+      if (MODE == kEpiScatterAdd || MODE == kEpiStoreRows) {
         valid = row_local < __ldg(p.plan.gsize + c.g);
         if (valid) {
           if (MODE == kEpiScatterAdd) {
@@ -353,6 +359,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
           }
           // 64-byte swizzle: 16-byte chunk j of row r lives at chunk j ^ ((r >> 1) & 3)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + off), "r"(hp[4 * j]),
+                         "r"(hp[4 * j + 1]), "r"(hp[4 * j + 2]), "r"(hp[4 * j + 3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.out, buf, col0 + cc * 32, c.mt * kTcBM + q * 32);
+            bulk_commit();
+          }
+        }
+      } else if (MODE == kEpiStoreBf16) {
+        // The tile's 128 x 256 fp32 accumulator as bf16 rows at its padded H
+        // rows (padding rows included: they fall inside the tile's own group),
+        // in 32 x 32 boxes through the same double-buffered 64-byte-swizzled
+        // staging as the gate-up's H stores. Boxes starting past the last
+        // column are skipped; TMA clips a box that straddles it.
+        const uint32_t buf0 = sStore + ew * 2 * kStoreBoxBytes;
+        const int32_t col0 = c.nt * kTcBN;
+#pragma unroll 1
+        for (int cc = 0; cc < kTcBN / 32 && col0 + cc * 32 < p.n_out; ++cc, ++nstore) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + cc * 32, v);
+          tmem_ld_wait();
+          uint32_t hp[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hp[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          const uint32_t buf = buf0 + (nstore & 1u) * kStoreBoxBytes;
+          if (nstore >= 2) {  // the store issued two boxes ago read this buffer
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
@@ -429,7 +470,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
     }
-    if (MODE == kEpiSwiGLU && lane == 0) bulk_wait<0>();
+    if (epi_stores_bf16(MODE) && lane == 0) bulk_wait<0>();
   }
 
   __syncthreads();

@@ -126,7 +126,7 @@ FfnWs ffn_layout(const moe_config* c) {
 
 struct FwdWs {
   size_t ids, w, counts, offsets, dest, perm_src, blk, rank, mt_start, gsize, a_row, o_row, x_perm,
-      H, y_acc, planes, total;
+      H, rows, planes, total;
 };
 FwdWs forward_layout(const moe_config* c) {
   Carver k;
@@ -147,7 +147,9 @@ FwdWs forward_layout(const moe_config* c) {
   w.o_row = k.take(sizeof(int32_t) * G);
   w.x_perm = k.take(act_bytes(c) * n * c->d);
   w.H = k.take(act_bytes(c) * padded_rows(c) * c->d_ff);
-  w.y_acc = c->act_dtype == MOE_DT_BF16 ? k.take(sizeof(float) * c->T * c->d) : 0;
+  // bf16 forward: the down projection's rows O [P, d] bf16 at padded H rows
+  // (the fp32 forward adds into y directly)
+  w.rows = c->act_dtype == MOE_DT_BF16 ? k.take(sizeof(__nv_bfloat16) * padded_rows(c) * c->d) : 0;
   w.planes = k.take(router_planes_bytes(c));
   w.total = k.off;
   return w;
@@ -200,6 +202,9 @@ moe_status device_state(DeviceState** out) {
     ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiScatterAdd>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(tc_smem_bytes(kEpiScatterAdd))) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiStoreBf16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tc_smem_bytes(kEpiStoreBf16))) == cudaSuccess;
 #define MOE_RTC_ATTR(NP)                                                                         \
   ok &= cudaFuncSetAttribute(router_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                              static_cast<int>(RtcShape<NP>::smem_bytes)) == cudaSuccess;
@@ -371,7 +376,7 @@ moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void
 // accumulator, zero_n4 float4s) on the side.
 moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void* x,
                           const void* x_perm, const GroupPlan& plan, const void* W1, const void* W3,
-                          const void* W2, void* H, int mode, float* out, const int32_t* perm_src,
+                          const void* W2, void* H, int mode, void* out, const int32_t* perm_src,
                           const float* topk_w, cudaStream_t st,
                           const std::function<moe_status(int)>* mark = nullptr,
                           float* zero = nullptr, int64_t zero_n4 = 0) {
@@ -394,7 +399,10 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
                      CU_TENSOR_MAP_SWIZZLE_128B));
     dn.a1 = dn.a0;
     dn.b1 = dn.b0;
-    dn.out = dn.a0;
+    if (mode == kEpiStoreBf16)
+      MOE_TRY(make_map(&dn.out, out, bf, 2, d, P, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
+    else
+      dn.out = dn.a0;
 
     TcArgs a{};
     a.plan = plan;
@@ -420,12 +428,15 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.n_tiles = (d + kTcBN - 1) / kTcBN;
     a.b_rows = d;
     a.n_out = d;
-    a.out = out;
+    a.out = mode == kEpiStoreBf16 ? nullptr : static_cast<float*>(out);
     a.zero_out = nullptr;
     a.zero_n4 = 0;
     // the combine folds the shared experts into one group (gate 1 for all)
-    a.fold_mt = (mode == kEpiScatterAdd && c->n_shared > 0) ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
-    if (mode == kEpiScatterAdd)
+    const bool fold = (mode == kEpiScatterAdd || mode == kEpiStoreBf16) && c->n_shared > 0;
+    a.fold_mt = fold ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
+    if (mode == kEpiStoreBf16)
+      grouped_gemm_tc<kEpiStoreBf16><<<grid, kTcThreads, tc_smem_bytes(kEpiStoreBf16), st>>>(dn, a);
+    else if (mode == kEpiScatterAdd)
       grouped_gemm_tc<kEpiScatterAdd><<<grid, kTcThreads, tc_smem_bytes(kEpiScatterAdd), st>>>(dn, a);
     else
       grouped_gemm_tc<kEpiStoreRows><<<grid, kTcThreads, tc_smem_bytes(kEpiStoreRows), st>>>(dn, a);
@@ -459,7 +470,7 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
   a.a1 = nullptr;
   a.b0 = static_cast<const float*>(W2);
   a.b1 = nullptr;
-  a.out = out;
+  a.out = static_cast<float*>(out);
   if (mode == kEpiScatterAdd)
     grouped_gemm_simt<kEpiScatterAdd><<<grid, kSimtThreads, 0, st>>>(a);
   else
@@ -671,7 +682,9 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, L.ids);
   float* w = topk_w_out ? topk_w_out : at<float>(workspace, L.w);
   int32_t* counts = counts_out ? counts_out : at<int32_t>(workspace, L.counts);
-  float* acc = bf ? at<float>(workspace, L.y_acc) : static_cast<float*>(y);
+  // bf16: the down projection's bf16 rows, summed per token by the combine
+  // kernel; fp32: the down projection adds straight into y
+  void* rows = bf ? at<void>(workspace, L.rows) : y;
 
   const std::function<moe_status(int)> mark = [&](int i) -> moe_status {
     if (stage_events == nullptr) return MOE_OK;
@@ -681,11 +694,10 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
     return MOE_ERR_CUDA;
   };
   MOE_TRY(mark(0));
-  // 1. gate
-  // (the fp32 router also clears y, the fp32 combine target; for bf16 the
-  // gate-up GEMM clears the accumulator)
+  // 1. gate (the fp32 router also clears y, the fp32 combine target)
   MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w,
-                       nullptr, bf ? nullptr : acc, ds->sm_count, at<void>(workspace, L.planes), st));
+                       nullptr, bf ? nullptr : static_cast<float*>(y), ds->sm_count,
+                       at<void>(workspace, L.planes), st));
   MOE_TRY(mark(1));
   // 2. dispatch + group plan
   PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
@@ -696,16 +708,19 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
                          at<int32_t>(workspace, L.rank), counts, at<int32_t>(workspace, L.offsets),
                          at<int32_t>(workspace, L.dest), perm_src, x_perm, &po, st));
   MOE_TRY(mark(2));
-  // 3. experts: gate-up + SwiGLU, then down with the gate-weighted scatter-add
+  // 3. experts: gate-up + SwiGLU, then the down projection (bf16 rows, or
+  // the gate-weighted scatter-add into y for fp32)
   GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
   MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H),
-                         kEpiScatterAdd, acc, perm_src, w, st, stage_events ? &mark : nullptr,
-                         bf ? acc : nullptr, cfg->T * cfg->d / 4));
-  // 4. fp32 accumulator -> bf16 output
+                         bf ? kEpiStoreBf16 : kEpiScatterAdd, rows, perm_src, w, st,
+                         stage_events ? &mark : nullptr));
+  // 4. bf16: y_t = shared row + sum_j g_{t,j} row(t, j), one warp per token
   if (bf) {
-    const int64_t n8 = cfg->T * cfg->d / 8;
-    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n8 + 255) / 256, 8ll * ds->sm_count));
-    cast_bf16_kernel<<<grid, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(y), n8);
+    const unsigned grid = static_cast<unsigned>((cfg->T + 7) / 8);
+    combine_rows_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(rows),
+                                                   at<int32_t>(workspace, L.dest), ids, w, po.mt_start,
+                                                   po.a_row, cfg->T, cfg->d, cfg->top_k, cfg->n_shared,
+                                                   static_cast<__nv_bfloat16*>(y));
     MOE_TRY(last_launch());
   }
   return mark(5);

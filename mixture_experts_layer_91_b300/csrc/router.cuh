@@ -37,7 +37,7 @@ struct RouterArgs {
   int32_t* topk_ids;     // [T, k]
   float* topk_w;         // [T, k]
   float* logits_out;     // [T, E] or null
-  float* zero_rows;      // [T, zero_width] fp32 rows to clear, or null (fused y_acc clear)
+  float* zero_rows;      // [T, zero_width] fp32 rows to clear, or null (the fp32 forward's y)
   int64_t T;
   int32_t d, E, k, renorm, noisy, zero_width;
   int32_t w_vec4;        // W rows may be copied in 16-byte pieces (E % 4 == 0, aligned)

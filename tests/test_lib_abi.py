@@ -99,10 +99,10 @@ def test_workspace_sizes_cover_the_buffers(lib, w):
     c = binding.config(w)
     ws = lib.moe_workspace_size(ctypes.byref(c))
     act = 4 if w.fp32 else 2
-    # at least x_perm + H (+ fp32 accumulator)
+    # at least x_perm + H (+ the down projection's bf16 rows)
     need = act * w.T * w.top_k * w.d + act * (w.n_shared * w.T + w.T * w.top_k) * w.d_ff
     if not w.fp32:
-        need += 4 * w.T * w.d
+        need += 2 * (w.n_shared * w.T + w.T * w.top_k) * w.d
     assert ws >= need
     assert lib.moe_permute_workspace_size(ctypes.byref(c)) >= 4 * w.T * w.top_k
     assert lib.moe_expert_ffn_workspace_size(ctypes.byref(c)) >= act * (w.n_shared * w.T + w.T * w.top_k) * w.d_ff
