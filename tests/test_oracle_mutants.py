@@ -32,6 +32,16 @@ def _topk_high_index_ties(key, k):
     return ids, kth - nxt
 
 
+def _topk_ascending_within_k(key, k):
+    ids, margin = _orig["topk_order"](key, k)
+    return ids[:, ::-1].copy(), margin          # the right set, listed by ascending key
+
+
+def _topk_margin_negated(key, k):
+    ids, margin = _orig["topk_order"](key, k)
+    return ids, -margin                          # (k+1)-th minus k-th
+
+
 def _softmax_wrong_axis(z):
     z = np.asarray(z, dtype=float)
     e = np.exp(z - z.max(axis=0, keepdims=True))
@@ -69,6 +79,21 @@ def _route_bias_in_gate(x, W_g, top_k, **kw):
     r = _orig["route"](x, W_g, top_k, **kw)
     if kw.get("bias") is not None:
         r["gates"] = r["gates"] + np.asarray(kw["bias"])[r["ids"]]
+    return r
+
+
+def _route_bias_on_logits(x, W_g, top_k, **kw):
+    # selection key logit + b instead of the score s + b
+    r = _orig["route"](x, W_g, top_k, **kw)
+    bias = kw.get("bias")
+    if bias is None:
+        return r
+    key = r["logits"] + np.asarray(bias, float)[None, :]
+    ids, margin = O.topk_order(key, top_k)
+    gates = np.take_along_axis(r["s"], ids, axis=1)
+    if kw.get("renormalize"):
+        gates = gates / gates.sum(axis=1, keepdims=True)
+    r.update(ids=ids, gates=gates, key=key, margin=margin)
     return r
 
 
@@ -127,6 +152,7 @@ def _run_pins():
         lambda: P.test_worked_example_closed_form(),
         lambda: P.test_noisy_gate_reductions(),
         lambda: P.test_bias_steers_selection_not_gates(),
+        lambda: P.test_bias_key_is_score_plus_bias_hand_values(),
         lambda: P.test_forward_matches_plain_loop_brute_force(False, 1, 5, 2),
         lambda: P.test_forward_matches_plain_loop_brute_force(True, 2, 6, 3),
         lambda: P.test_sparse_equals_dense(),
@@ -154,12 +180,15 @@ def _run_pins():
 MUTANTS = {
     "silu_as_relu": ("silu", _silu_relu),
     "topk_ties_high_index": ("topk_order", _topk_high_index_ties),
+    "topk_ascending_within_k": ("topk_order", _topk_ascending_within_k),
+    "topk_margin_negated": ("topk_order", _topk_margin_negated),
     "softmax_wrong_axis": ("softmax", _softmax_wrong_axis),
     "ffn_gate_up_swapped": ("expert_ffn", _ffn_swapped),
     "ffn_w2_reinterpreted": ("expert_ffn", _ffn_w2_transposed),
     "forward_drops_shared": ("moe_forward", _forward_no_shared),
     "route_ignores_renorm": ("route", _route_no_renorm),
     "route_bias_in_gate": ("route", _route_bias_in_gate),
+    "route_bias_on_logits": ("route", _route_bias_on_logits),
     "dispatch_unstable": ("dispatch", _dispatch_descending),
     "combine_gates_flipped": ("combine", _combine_flipped_gates),
     "softplus_as_exp": ("softplus", _softplus_exp),

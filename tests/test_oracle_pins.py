@@ -209,6 +209,24 @@ def test_bias_steers_selection_not_gates():
     np.testing.assert_allclose(r0["gates"], rp["gates"], rtol=1e-15)
 
 
+def test_bias_key_is_score_plus_bias_hand_values():
+    """The biased selection key is s_i + b_i, the softmax score plus the bias.
+    The page on the auxiliary-loss-free strategy says only that a per-expert
+    bias steers the assignment; adding it to the score (not the logit) is the
+    reading taken, and this pins it. One token with logits (2, 0, -1) and
+    b = (0, 0.9, 0):
+    s = (e^2, 1, e^-1) / (e^2 + 1 + e^-1) = (0.8438, 0.1142, 0.0420), so
+    s + b = (0.8438, 1.0142, 0.0420) ranks expert 1 first and expert 0 second,
+    where logit + b = (2, 0.9, -1) would rank 0 first. Gates are s of the picks."""
+    x = np.array([[1.0]])
+    W_g = np.array([[2.0, 0.0, -1.0]])
+    r = O.route(x, W_g, 2, bias=np.array([0.0, 0.9, 0.0]))
+    z = math.exp(2.0) + 1.0 + math.exp(-1.0)
+    assert r["ids"].tolist() == [[1, 0]]
+    np.testing.assert_allclose(r["gates"], [[1.0 / z, math.exp(2.0) / z]], rtol=1e-14)
+    np.testing.assert_allclose(r["margin"], [math.exp(2.0) / z - math.exp(-1.0) / z], rtol=1e-13)
+
+
 # ---------------------------------------------------------------- layer output
 
 @pytest.mark.parametrize("renorm", [False, True])
