@@ -3,7 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step is one whole layer forward (router, dispatch, gate-up GEMM with
-SwiGLU, down GEMM, gate-weighted combine) over one batch of
+SwiGLU, down GEMM, gate-weighted combine: bf16 expert rows summed per token
+by a combine kernel, or with --workload dsmoe16b_scatter_T16384 the down
+GEMM's scatter-add into an fp32 accumulator and a cast) over one batch of
 T synthetic tokens, inputs resident in HBM. Default workload: the
 DeepSeekMoE-16B-shaped layer at T = 16384 tokens. With N > 1 (torchrun) every
 rank runs an independent replica on its own GPU (the layer's tokens are
@@ -260,6 +262,7 @@ def workload_config(w, world: int, ab: float | None = None) -> dict:
            "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
            "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
            "expert": w.act, "capacity": w.capacity or None,
+           "combine": "fp32 scatter-add" if (w.fp32 or w.combine == "scatter") else "bf16 rows + combine kernel",
            "parallelism": f"replicas x{world}"}
     if ab is not None:
         cfg["l2"] = f"inputs larger than L2: {ab / 2**20:.0f} MiB of weights+activations per step"
@@ -355,7 +358,10 @@ def main():
         raise RuntimeError(f"device fault flag {raw} after the timed region")
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
-    stage_names = ["router", "dispatch", "gate_up", "down", "combine"]
+    # last stage: the combine kernel over bf16 rows, or the cast of the fp32
+    # scatter-add accumulator (empty for fp32 layers, which add into y)
+    stage_names = ["router", "dispatch", "gate_up", "down",
+                   "cast" if (not w.fp32 and w.combine == "scatter") else "combine"]
     stage_ms = {n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_ev)
                 for j, n in enumerate(stage_names)}
 
@@ -388,7 +394,7 @@ def main():
     tflops = world * flops / (ms_step / 1e3) / 1e12
     ab = algorithmic_bytes(w, touched)
     roof_time = max(flops / (pk["bf16_tflops"] * 1e12), ab / (pk["hbm_gbs"] * 1e9))
-    # bf16: [W split] + router + count + scan + rank + gate-up + down + combine;
+    # bf16: [W split] + router + count + scan + rank + gate-up + down + (combine | cast);
     # fp32: router + count + scan + scatter + gate-up + down
     tc_router = (not w.fp32) and (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
     launches_per_step = 6 if w.fp32 else (8 if tc_router else 7)

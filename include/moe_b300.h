@@ -76,12 +76,32 @@ typedef struct {
   int32_t act_dtype;   /* moe_dtype                                              */
   int32_t capacity;    /* max assignments an expert accepts, 0 = no limit        */
   int32_t expert_act;  /* moe_expert_act                                         */
+  int32_t combine;     /* moe_combine_mode (bf16 layers; fp32 layers scatter-add) */
 } moe_config;
 
 typedef enum {
   MOE_ACT_SWIGLU = 0,  /* FFN(u) = W2 (silu(W1 u) * (W3 u))                       */
   MOE_ACT_RELU = 1     /* FFN(u) = W2 ReLU(W1 u) (GShard's wo.ReLU(wi.x)); W3 unused */
 } moe_expert_act;
+
+/*
+ * How moe_forward forms y_t = sum_shared FFN_i(u_t) + sum_j g_{t,j} FFN_j(u_t)
+ * (DeepSeekMoE translation on gitcode.csdn.net, section 3.2, eq (9)) in bf16
+ * layers. Both sum in fp32 and round y once to bf16; they differ in where the
+ * expert rows meet:
+ *   MOE_COMBINE_ROWS: the down GEMM stores every expert row FFN_e(u_t) as bf16
+ *     (the K_s shared experts summed into one row per token), and a combine
+ *     kernel adds each token's rows with their gates in a fixed order.
+ *     Deterministic; each row is rounded to bf16 before the sum.
+ *   MOE_COMBINE_SCATTER_ADD: the down GEMM's epilogue adds g * FFN_e(u_t) into
+ *     an fp32 accumulator with fp32 atomics (shared experts at gate 1), cast to
+ *     y at the end. The rows stay fp32; the atomics' order varies run to run.
+ * fp32 layers always add straight into y (the scatter-add form).
+ */
+typedef enum {
+  MOE_COMBINE_ROWS = 0,
+  MOE_COMBINE_SCATTER_ADD = 1
+} moe_combine_mode;
 
 /*
  * Expert capacity ("Mixture of Experts" notes, section 3, GShard expert
@@ -249,22 +269,18 @@ size_t moe_workspace_size(const moe_config* cfg);
 
 /*
  * moe_forward -- the whole layer: route, dispatch, grouped SwiGLU experts and
- * the gate-weighted combine ([DSMoE] section 3.2, eq (9)), fused as: router
- * -> histogram/scan/plan -> gather -> gate-up GEMM with SiLU*up fused ->
- * down GEMM -> combine. bf16 layers: the down GEMM stores each expert row
- * FFN_e(u_t) as bf16 (the K_s shared experts summed into one row per token),
- * and the combine kernel forms y_t = shared row + sum_j g_{t,j} row(t, j) in
- * fp32, in a fixed order, rounded once to bf16. fp32 layers: the down GEMM
- * adds g * FFN into y with fp32 atomics. Arguments as in moe_route /
- * moe_expert_ffn. ([DSMoE]: the DeepSeekMoE paper, Chinese translation on
- * gitcode.csdn.net.)
+ * the gate-weighted combine (DeepSeekMoE translation on gitcode.csdn.net,
+ * section 3.2, eq (9)), fused as: router -> histogram/scan/plan -> gather ->
+ * gate-up GEMM with SiLU*up fused -> down GEMM -> combine, the last two as
+ * cfg->combine selects (moe_combine_mode). Arguments as in moe_route /
+ * moe_expert_ffn.
  *   y            [T, d]  act_dtype (out)
  *   topk_ids_out [T, k]  int32 or NULL (out) routing decisions
  *   topk_w_out   [T, k]  fp32  or NULL (out) gate values
  *   counts_out   [N_r]   int32 or NULL (out) tokens per routed expert
- * bf16 layers give the same y on every run; in fp32 layers the atomics'
- * summation order of a token's k + K_s contributions (not the result's
- * tolerance) varies run to run.
+ * MOE_COMBINE_ROWS gives the same y on every run; with the scatter-add (and
+ * in fp32 layers) the atomics' summation order of a token's k + K_s
+ * contributions (not the result's tolerance) varies run to run.
  */
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
                        const float* W_noise, const float* eps, const float* bias,
@@ -283,8 +299,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
  * MOE_PROFILE_EVENTS cudaEvent_t handles (or is NULL, which makes the call
  * identical to moe_forward): [0] before the router, [1] after the router,
  * [2] after dispatch (count, scan+plan, gather), [3] after the gate-up GEMM,
- * [4] after the down GEMM, [5] after the combine into y (bf16 layers; for
- * fp32 layers the down GEMM's scatter-add already formed y).
+ * [4] after the down GEMM, [5] after the combine kernel or the cast to y
+ * (bf16 layers; for fp32 layers the down GEMM's scatter-add already formed y).
  */
 moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const float* W_g,
                                 const float* W_noise, const float* eps, const float* bias,

@@ -45,6 +45,7 @@ class MoeError(RuntimeError):
 
 
 MOE_ACT_SWIGLU, MOE_ACT_RELU = 0, 1
+MOE_COMBINE_ROWS, MOE_COMBINE_SCATTER_ADD = 0, 1
 
 
 class MoeConfig(ctypes.Structure):
@@ -52,7 +53,7 @@ class MoeConfig(ctypes.Structure):
                 ("n_shared", ctypes.c_int32), ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("gate", ctypes.c_int32),
                 ("act_dtype", ctypes.c_int32), ("capacity", ctypes.c_int32),
-                ("expert_act", ctypes.c_int32)]
+                ("expert_act", ctypes.c_int32), ("combine", ctypes.c_int32)]
 
 
 class RouterStats(ctypes.Structure):
@@ -64,7 +65,8 @@ def config(w: Workload, T: int | None = None) -> MoeConfig:
                      top_k=w.top_k, d_ff=w.d_ff, renormalize=int(w.renormalize or w.noisy),
                      gate=MOE_GATE_NOISY if w.noisy else MOE_GATE_SOFTMAX,
                      act_dtype=MOE_DT_F32 if w.fp32 else MOE_DT_BF16, capacity=w.capacity,
-                     expert_act=MOE_ACT_RELU if w.act == "relu" else MOE_ACT_SWIGLU)
+                     expert_act=MOE_ACT_RELU if w.act == "relu" else MOE_ACT_SWIGLU,
+                     combine=MOE_COMBINE_SCATTER_ADD if w.combine == "scatter" else MOE_COMBINE_ROWS)
 
 
 def load(path: str = _LIB_PATH) -> ctypes.CDLL:

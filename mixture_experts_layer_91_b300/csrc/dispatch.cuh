@@ -318,6 +318,22 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// fp32 accumulator -> bf16 output, 8 elements per thread per step.
+__global__ void __launch_bounds__(256)
+    cast_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n8) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(src) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 2 * i + 1);
+    uint4 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4*>(dst)[i] = o;
+  }
+}
+
 // Test hook: a wait on an mbarrier that nothing arrives on, bounded by limit_ns.
 __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;

@@ -24,7 +24,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kVersion = (2 << 16) | 0;
+constexpr int kVersion = (2 << 16) | 1;
 constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
@@ -44,6 +44,7 @@ moe_status check_config(const moe_config* c) {
   if (c->gate == MOE_GATE_NOISY && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
   if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
   if (c->expert_act != MOE_ACT_SWIGLU && c->expert_act != MOE_ACT_RELU) return MOE_ERR_INVALID_ARG;
+  if (c->combine != MOE_COMBINE_ROWS && c->combine != MOE_COMBINE_SCATTER_ADD) return MOE_ERR_INVALID_ARG;
   if (c->d % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
   const int cols = c->gate == MOE_GATE_NOISY ? 2 * c->n_routed : c->n_routed;
   if (cols > 256 || c->top_k > 32 || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
@@ -55,6 +56,12 @@ moe_status check_config(const moe_config* c) {
 }
 
 size_t act_bytes(const moe_config* c) { return c->act_dtype == MOE_DT_BF16 ? 2 : 4; }
+
+// bf16 layers combining through stored bf16 expert rows (else: the fp32
+// scatter-add, which fp32 layers always use)
+bool rows_combine(const moe_config* c) {
+  return c->act_dtype == MOE_DT_BF16 && c->combine == MOE_COMBINE_ROWS;
+}
 
 constexpr int64_t kRouterTcMinTokens = 4096;
 
@@ -126,7 +133,7 @@ FfnWs ffn_layout(const moe_config* c) {
 
 struct FwdWs {
   size_t ids, w, counts, offsets, dest, perm_src, blk, rank, mt_start, gsize, a_row, o_row, x_perm,
-      H, rows, planes, total;
+      H, y_acc, rows, planes, total;
 };
 FwdWs forward_layout(const moe_config* c) {
   Carver k;
@@ -147,9 +154,11 @@ FwdWs forward_layout(const moe_config* c) {
   w.o_row = k.take(sizeof(int32_t) * G);
   w.x_perm = k.take(act_bytes(c) * n * c->d);
   w.H = k.take(act_bytes(c) * padded_rows(c) * c->d_ff);
-  // bf16 forward: the down projection's rows O [P, d] bf16 at padded H rows
-  // (the fp32 forward adds into y directly)
-  w.rows = c->act_dtype == MOE_DT_BF16 ? k.take(sizeof(__nv_bfloat16) * padded_rows(c) * c->d) : 0;
+  // bf16 layers: the scatter-add's fp32 accumulator [T, d], or the down
+  // projection's bf16 rows O [P, d] at padded H rows (fp32 layers add into y)
+  const bool bf = c->act_dtype == MOE_DT_BF16;
+  w.y_acc = bf && !rows_combine(c) ? k.take(sizeof(float) * c->T * c->d) : 0;
+  w.rows = rows_combine(c) ? k.take(sizeof(__nv_bfloat16) * padded_rows(c) * c->d) : 0;
   w.planes = k.take(router_planes_bytes(c));
   w.total = k.off;
   return w;
@@ -682,9 +691,12 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, L.ids);
   float* w = topk_w_out ? topk_w_out : at<float>(workspace, L.w);
   int32_t* counts = counts_out ? counts_out : at<int32_t>(workspace, L.counts);
-  // bf16: the down projection's bf16 rows, summed per token by the combine
-  // kernel; fp32: the down projection adds straight into y
-  void* rows = bf ? at<void>(workspace, L.rows) : y;
+  // The down projection's target: bf16 rows summed per token by the combine
+  // kernel (MOE_COMBINE_ROWS), or the fp32 accumulator of the scatter-add
+  // (y_acc for bf16, y itself for fp32).
+  const bool by_rows = rows_combine(cfg);
+  float* acc = by_rows ? nullptr : (bf ? at<float>(workspace, L.y_acc) : static_cast<float*>(y));
+  void* rows = by_rows ? at<void>(workspace, L.rows) : nullptr;
 
   const std::function<moe_status(int)> mark = [&](int i) -> moe_status {
     if (stage_events == nullptr) return MOE_OK;
@@ -708,19 +720,29 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
                          at<int32_t>(workspace, L.rank), counts, at<int32_t>(workspace, L.offsets),
                          at<int32_t>(workspace, L.dest), perm_src, x_perm, &po, st));
   MOE_TRY(mark(2));
-  // 3. experts: gate-up + SwiGLU, then the down projection (bf16 rows, or
-  // the gate-weighted scatter-add into y for fp32)
+  // 3. experts: gate-up + SwiGLU, then the down projection: bf16 rows, or
+  // the gate-weighted scatter-add (for bf16 the gate-up GEMM clears y_acc)
   GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
-  MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H),
-                         bf ? kEpiStoreBf16 : kEpiScatterAdd, rows, perm_src, w, st,
-                         stage_events ? &mark : nullptr));
-  // 4. bf16: y_t = shared row + sum_j g_{t,j} row(t, j), one warp per token
-  if (bf) {
+  if (by_rows)
+    MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H), kEpiStoreBf16,
+                           rows, perm_src, w, st, stage_events ? &mark : nullptr));
+  else
+    MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, at<void>(workspace, L.H), kEpiScatterAdd,
+                           acc, perm_src, w, st, stage_events ? &mark : nullptr, bf ? acc : nullptr,
+                           cfg->T * cfg->d / 4));
+  // 4. y_t = shared row + sum_j g_{t,j} row(t, j), one warp per token; or the
+  // fp32 accumulator -> bf16 y
+  if (by_rows) {
     const unsigned grid = static_cast<unsigned>((cfg->T + 7) / 8);
     combine_rows_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(rows),
                                                    at<int32_t>(workspace, L.dest), ids, w, po.mt_start,
                                                    po.a_row, cfg->T, cfg->d, cfg->top_k, cfg->n_shared,
                                                    static_cast<__nv_bfloat16*>(y));
+    MOE_TRY(last_launch());
+  } else if (bf) {
+    const int64_t n8 = cfg->T * cfg->d / 8;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n8 + 255) / 256, 8ll * ds->sm_count));
+    cast_bf16_kernel<<<grid, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(y), n8);
     MOE_TRY(last_launch());
   }
   return mark(5);

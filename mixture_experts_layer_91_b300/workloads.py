@@ -35,6 +35,7 @@ class Workload:
     seed: int = 91
     capacity: int = 0           # assignments an expert accepts (0 = dropless)
     act: str = "swiglu"         # expert FFN: "swiglu" or GShard's "relu" (no W3)
+    combine: str = "rows"       # bf16 combine: "rows" (bf16 expert rows + combine kernel) or "scatter"
 
     @property
     def n_experts(self) -> int:
@@ -80,7 +81,13 @@ DSMOE_145B_DECODE = replace(DSMOE_145B, name="dsmoe145b_decode_T64", T=64)
 GSHARD_RELU_CAP = replace(GSHARD_NOISY, name="gshard_relu_cap1.25_T16384", act="relu",
                           capacity=-(-5 * 16384 * 2 // (4 * 16)), seed=96)
 
-ALL = [TINY_FP32, DSMOE_2B, DSMOE_16B, GSHARD_NOISY, DSMOE_145B, DSMOE_145B_DECODE, GSHARD_RELU_CAP]
+# The headline layer with the down projection's gate-weighted scatter-add into
+# an fp32 accumulator (moe_combine_mode MOE_COMBINE_SCATTER_ADD) instead of
+# stored bf16 expert rows; same inputs.
+DSMOE_16B_SCATTER = replace(DSMOE_16B, name="dsmoe16b_scatter_T16384", combine="scatter")
+
+ALL = [TINY_FP32, DSMOE_2B, DSMOE_16B, GSHARD_NOISY, DSMOE_145B, DSMOE_145B_DECODE, GSHARD_RELU_CAP,
+       DSMOE_16B_SCATTER]
 BY_NAME = {w.name: w for w in ALL}
 
 # the layer the throughput headline is quoted on: the 16B-shaped layer at 16K tokens

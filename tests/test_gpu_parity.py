@@ -382,3 +382,37 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     assert st == 5 and raw & 1
     assert binding.device_status()[0] == 0
     test_forward_small(workloads.TINY_FP32, cuda_lib)   # the context is still usable
+
+
+# ------------------------------------------------------------------ combine modes
+# The layers above run the default MOE_COMBINE_ROWS (bf16 expert rows summed per
+# token by the combine kernel); these run the down GEMM's gate-weighted
+# scatter-add into an fp32 accumulator (MOE_COMBINE_SCATTER_ADD). Same names and
+# inputs as their row-combine twins.
+SCATTER = [workloads.replace(w, combine="scatter") for w in
+           (workloads.DSMOE_16B.with_tokens(333), GSHARD_RELU_SMALL, RAGGED, DSMOE_16B_CAP,
+            workloads.DSMOE_145B_DECODE)]
+
+
+@pytest.mark.parametrize("w", SCATTER, ids=lambda w: w.name + "_scatter")
+def test_forward_scatter_add_combine(w, cuda_lib):
+    forward_case(w, None)
+
+
+def test_forward_scatter_add_combine_full_size(cuda_lib):
+    forward_case(workloads.DSMOE_16B_SCATTER, 1024)
+
+
+def test_combine_modes_agree_and_rows_are_bitwise_repeatable(cuda_lib):
+    w = workloads.DSMOE_16B.with_tokens(333)
+    inp = get_inputs(w)
+    g = {k: dev(v) for k, v in inp.items()}
+
+    def run(wl):
+        return binding.forward(binding.config(wl), g["x"], g["W_g"], g["W_noise"], g["eps"], g["bias"],
+                               g["W1"], g["W3"], g["W2"]).float().cpu().numpy()
+
+    y_rows, y_rows2 = run(w), run(w)
+    y_scatter = run(workloads.replace(w, combine="scatter"))
+    assert np.array_equal(y_rows, y_rows2), "the row combine is not deterministic"
+    check_close(y_rows, y_scatter, False, "rows vs scatter-add")

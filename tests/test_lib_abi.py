@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.moe_version() >> 16 == 2
+    assert lib.moe_version() >> 16 == 2 and lib.moe_version() & 0xffff >= 1
     for s in range(8):
         assert lib.moe_status_string(s).startswith(b"MOE_")
     assert b"unknown" in lib.moe_status_string(99)
@@ -63,7 +63,7 @@ def cfg_of(**kw):
 @pytest.mark.parametrize("bad", [
     dict(top_k=17), dict(top_k=0), dict(d=0), dict(T=-1), dict(n_routed=0), dict(gate=2),
     dict(act_dtype=5), dict(renormalize=2), dict(gate=1, renormalize=0), dict(capacity=-1),
-    dict(expert_act=2),
+    dict(expert_act=2), dict(combine=2), dict(combine=-1),
 ])
 def test_invalid_configs_rejected(lib, bad):
     c = cfg_of(**bad)
@@ -99,10 +99,11 @@ def test_workspace_sizes_cover_the_buffers(lib, w):
     c = binding.config(w)
     ws = lib.moe_workspace_size(ctypes.byref(c))
     act = 4 if w.fp32 else 2
-    # at least x_perm + H (+ the down projection's bf16 rows)
+    # at least x_perm + H (+ the down projection's bf16 rows, or the fp32
+    # accumulator of the scatter-add combine)
     need = act * w.T * w.top_k * w.d + act * (w.n_shared * w.T + w.T * w.top_k) * w.d_ff
     if not w.fp32:
-        need += 2 * (w.n_shared * w.T + w.T * w.top_k) * w.d
+        need += 4 * w.T * w.d if w.combine == "scatter" else 2 * (w.n_shared * w.T + w.T * w.top_k) * w.d
     assert ws >= need
     assert lib.moe_permute_workspace_size(ctypes.byref(c)) >= 4 * w.T * w.top_k
     assert lib.moe_expert_ffn_workspace_size(ctypes.byref(c)) >= act * (w.n_shared * w.T + w.T * w.top_k) * w.d_ff
@@ -142,3 +143,30 @@ def test_relu_experts_take_no_w3_but_swiglu_needs_it(lib):
         st = lib.moe_forward(ctypes.byref(c), fake, fake, None, None, None, fake, None, fake, fake, 16,
                              fake, None, None, None, None)
         assert st == want
+
+
+def test_workspace_follows_the_combine_mode(lib):
+    """bf16 layers: MOE_COMBINE_ROWS takes the bf16 rows O [P, d] (P the padded
+    H rows), MOE_COMBINE_SCATTER_ADD the fp32 accumulator [T, d]; fp32 layers
+    add into y and need neither, whatever the mode."""
+    T, d, E, K_s, k, I = 4096, 256, 16, 1, 4, 64
+    P = K_s * ((T + 127) // 128) * 128 + T * k + 128 * E
+    base = dict(T=T, d=d, n_routed=E, n_shared=K_s, top_k=k, d_ff=I)
+    rows = lib.moe_workspace_size(ctypes.byref(cfg_of(**base, act_dtype=1, combine=0)))
+    scat = lib.moe_workspace_size(ctypes.byref(cfg_of(**base, act_dtype=1, combine=1)))
+    assert rows - scat == 2 * P * d - 4 * T * d
+    f0 = lib.moe_workspace_size(ctypes.byref(cfg_of(**base, act_dtype=0, combine=0)))
+    f1 = lib.moe_workspace_size(ctypes.byref(cfg_of(**base, act_dtype=0, combine=1)))
+    assert f0 == f1 > 0
+    assert binding.MOE_COMBINE_ROWS == 0 and binding.MOE_COMBINE_SCATTER_ADD == 1
+    assert binding.config(workloads.DSMOE_16B).combine == binding.MOE_COMBINE_ROWS
+    assert binding.config(workloads.DSMOE_16B_SCATTER).combine == binding.MOE_COMBINE_SCATTER_ADD
+
+
+def test_config_struct_matches_the_header():
+    """The ctypes mirror of moe_config lists the header's fields in order."""
+    src = open(HEADER).read()
+    body = src[src.index("typedef struct {\n  int64_t T;"):]
+    body = body[:body.index("} moe_config;")]
+    names = re.findall(r"\b(?:int64_t|int32_t)\s+(\w+);", body)
+    assert names == [f[0] for f in binding.MoeConfig._fields_]
