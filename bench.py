@@ -152,11 +152,38 @@ class ClockSampler:
 KERNEL_SOURCES = ("gemm_tc.cuh", "common.cuh")   # the gate-up kernel and the device helpers it inlines
 
 
+def code_tokens(src: str) -> str:
+    """C++ source with its comments removed and whitespace runs collapsed:
+    what the compiler sees, so an edit to comments alone keeps the key."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":                     # string / char literal, escapes kept
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha() -> str:
+    """Key of the gate-up kernel's code (comments and layout excluded) that the
+    committed traffic record was captured on."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "mixture_experts_layer_91_b300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mixture_experts_layer_91_b300", "csrc", name), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

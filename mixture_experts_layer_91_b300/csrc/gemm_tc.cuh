@@ -18,17 +18,20 @@
 //   warp 1      allocates 512 TMEM columns; one thread issues
 //               tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of two
 //               TMEM accumulators and commits stage / accumulator barriers.
-//   warps 2..5  epilogue: (gate-up, forward path: first clear a share of the
-//               fp32 combine accumulator while the first MMAs run) then
-//               tcgen05.ld of the accumulator (each warp owns one
+//   warps 2..5  epilogue: (gate-up with the scatter-add combine: first clear
+//               a share of the fp32 combine accumulator while the first MMAs
+//               run) then tcgen05.ld of the accumulator (each warp owns one
 //               32-lane quarter), then
 //                 gate-up : h = silu(acc[:, 0:128]) * acc[:, 128:256] -> bf16
 //                           (GShard ReLU experts: h = relu(acc[:, 0:256])),
 //                           staged in shared memory, TMA-stored to H;
-//                 down    : acc * gate, transposed in registers so each warp
-//                           instruction adds one 128-byte row segment
-//                           (red.global.add.f32) into y_acc[token]; or stored
-//                           as fp32 rows (stage entry point).
+//                 down    : acc -> bf16, staged and TMA-stored at the tile's
+//                           padded H rows for the per-token combine kernel
+//                           (StoreBf16); or acc * gate, transposed in
+//                           registers so each warp instruction adds one
+//                           128-byte row segment (red.global.add.f32) into
+//                           y_acc[token] (ScatterAdd); or stored as fp32 rows
+//                           (StoreRows, stage entry point).
 //
 // The gate-up B tile stacks 128 rows of W1 over the same 128 rows of W3, so
 // one N=256 MMA produces the gate and up halves of the same output columns

@@ -54,3 +54,12 @@ def test_traffic_record_applies_only_to_its_workload():
         assert rec["workload"] == workloads.DSMOE_16B.name
     for w in (workloads.DSMOE_145B_DECODE, workloads.GSHARD_NOISY, workloads.DSMOE_2B):
         assert bench.ncu_traffic(w) is None
+
+
+def test_kernel_key_ignores_comments_but_not_code():
+    a = 'int f(int x) { // doubles\n  return 2 * x;  /* fast */ }\nconst char* s = "a // b";\n'
+    b = 'int f(int x) {   // returns twice x\n  return 2 * x; }\nconst char* s = "a // b";\n'
+    c = 'int f(int x) { return 3 * x; }\nconst char* s = "a // b";\n'
+    assert bench.code_tokens(a) == bench.code_tokens(b)
+    assert bench.code_tokens(a) != bench.code_tokens(c)
+    assert '"a // b"' in bench.code_tokens(a)        # a // inside a string literal is code
