@@ -227,36 +227,57 @@ def gate_up_roofline(w, touched: int, kept: int, gate_up_ms: float, pk: dict, pk
             "frac": achieved / hbm_peak, "peak_kind": f"{pk_kind} copy bandwidth", **common}
 
 
-def cpu_oracle_rate(w, inp, budget_s: float) -> dict:
-    """The fp64 oracle (route + sparse SwiGLU experts) on a bounded token sample."""
-    from oracle import moe_oracle as O
+ORACLE_SAMPLE_TOKENS = 4096
+
+
+def oracle_sample(w) -> np.ndarray:
+    """The fixed, seeded token sample one oracle step runs on: all tokens of a
+    small layer, else ORACLE_SAMPLE_TOKENS of them (tokens are independent and
+    the layer is dropless, so a sample's rows are exact)."""
+    n = min(ORACLE_SAMPLE_TOKENS, w.T)
+    return np.sort(np.random.default_rng(0).choice(w.T, n, replace=False))
+
+
+def oracle_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:  # noqa: BLE001
-        cores = os.cpu_count() or 1
-    rng = np.random.default_rng(0)
+        return os.cpu_count() or 1
 
-    def run(n):
-        toks = np.sort(rng.choice(w.T, n, replace=False))
-        x = inp["x"][torch.from_numpy(toks)]
-        eps = inp["eps"][torch.from_numpy(toks)] if inp["eps"] is not None else None
-        t0 = time.perf_counter()
-        r = O.route(x, inp["W_g"], w.top_k, renormalize=w.renormalize, noisy=w.noisy,
-                    W_noise=inp["W_noise"], eps=eps, bias=inp["bias"])
-        O.moe_forward(x, inp["W1"], inp["W3"], inp["W2"], w.n_shared, r["ids"], r["gates"])
-        return time.perf_counter() - t0
 
-    n = min(64, w.T)
-    dt = run(n)   # also warms up the BLAS thread pool
-    for _ in range(3):   # grow the sample toward the time budget; report the last run
-        if dt >= budget_s / 2 or n >= w.T:
-            break
-        n = int(min(w.T, max(2 * n, n * budget_s / max(dt, 1e-3))))
-        dt = run(n)
-    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.T} tokens of {w.name}: fp64 route + sparse SwiGLU experts "
-                      f"(numpy/BLAS), {dt:.1f} s"}
+def oracle_step(w, inp, toks) -> float:
+    """One step of the fp64 CPU oracle, as it stands: route the sampled tokens
+    and run their sparse SwiGLU (or ReLU) experts. Returns its wall time in s.
+    The oracle widens every expert's weights to fp64 on each call, a fixed cost
+    per step that the sample size amortises."""
+    from oracle import moe_oracle as O
+    idx = torch.from_numpy(toks)
+    x = inp["x"][idx]
+    eps = inp["eps"][idx] if inp["eps"] is not None else None
+    t0 = time.perf_counter()
+    r = O.route(x, inp["W_g"], w.top_k, renormalize=w.renormalize, noisy=w.noisy,
+                W_noise=inp["W_noise"], eps=eps, bias=inp["bias"])
+    keep = O.capacity_keep(r["ids"], w.n_routed, w.capacity) if w.capacity else None
+    O.moe_forward(x, inp["W1"], inp["W3"], inp["W2"], w.n_shared, r["ids"], r["gates"], act=w.act,
+                  keep=keep)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_note(w, n: int, secs: list) -> str:
+    what = "SwiGLU" if w.act != "relu" else "ReLU"
+    return (f"{n} of {w.T} tokens of {w.name} per step (fixed seeded sample): fp64 route + sparse "
+            f"{what} experts (numpy/BLAS); {len(secs)} timed steps of {statistics.mean(secs):.2f} s")
+
+
+def cpu_oracle_rate(w, inp, steps: int = 3) -> dict:
+    """cpu_baseline: the oracle on the bench's fixed token sample, one untimed
+    step then `steps` timed ones (the same steps `--impl reference` times)."""
+    toks = oracle_sample(w)
+    oracle_step(w, inp, toks)   # warms the BLAS thread pool
+    secs = [oracle_step(w, inp, toks) for _ in range(steps)]
+    return {"value": toks.size / statistics.median(secs), "unit": "tokens/s", "cores": oracle_threads(),
+            "kind": "oracle", "sample": oracle_sample_note(w, toks.size, secs)}
 
 
 def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
@@ -283,37 +304,48 @@ def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
     return max_over_ranks(e_start.elapsed_time(e_end) / n, world, dev)
 
 
-def workload_config(w, world: int, ab: float | None = None) -> dict:
+def resident_bytes(w) -> int:
+    """Bytes one step reads from HBM at the least: every expert's weights
+    (all are touched in a dropless prefill batch), x and y."""
+    act = 4 if w.fp32 else 2
+    return w.n_experts * w.n_mats * w.d * w.d_ff * act + 2 * w.T * w.d * act
+
+
+def workload_config(w, world: int) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
-    cfg = {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
-           "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
-           "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
-           "expert": w.act, "capacity": w.capacity or None,
-           "combine": "fp32 scatter-add" if (w.fp32 or w.combine == "scatter") else "bf16 rows + combine kernel",
-           "parallelism": f"replicas x{world}"}
-    if ab is not None:
-        cfg["l2"] = f"inputs larger than L2: {ab / 2**20:.0f} MiB of weights+activations per step"
-    return cfg
+    rb = resident_bytes(w)
+    l2 = (f"inputs larger than L2: {rb / 2**20:.0f} MiB of expert weights + x + y per step"
+          if rb > L2_BYTES else f"inputs fit in L2 ({rb / 2**20:.0f} MiB): warm-L2 figure")
+    return {"workload": w.name, "T": w.T, "d": w.d, "n_routed": w.n_routed,
+            "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
+            "gate": "noisy" if w.noisy else ("softmax+bias" if w.bias else "softmax"),
+            "expert": w.act, "capacity": w.capacity or None,
+            "combine": "fp32 scatter-add" if (w.fp32 or w.combine == "scatter") else "bf16 rows + combine kernel",
+            "parallelism": f"replicas x{world}", "l2": l2}
 
 
 def run_reference(args, w):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores.
+    One step = one oracle pass over the fixed token sample; warm-up steps run
+    untimed; value = sampled tokens / median step time; ms_per_step is the
+    measured wall time of a step (what ran, not an extrapolation)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     inp = inputs.make_inputs(w)
-    budget = 20.0
-    steps = []
-    for _ in range(args.warmup + args.steps):
-        steps.append(cpu_oracle_rate(w, inp, budget / max(1, args.steps + args.warmup)))
-    timed = steps[args.warmup:]
-    val = statistics.median(s["value"] for s in timed)
+    toks = oracle_sample(w)
+    for _ in range(args.warmup):
+        oracle_step(w, inp, toks)
+    secs = [oracle_step(w, inp, toks) for _ in range(args.steps)]
+    val = toks.size / statistics.median(secs)
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * w.T / val,   # one step = the workload's T tokens at the sampled rate
+            "ms_per_step": 1e3 * statistics.mean(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; no checkpoint)",
             "config": workload_config(w, world),
-            "cpu_baseline": {**timed[-1], "value": val},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+                             "sample": oracle_sample_note(w, toks.size, secs)},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -431,7 +463,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.fp32 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; no checkpoint)",
-        "config": workload_config(w, world, ab),
+        "config": workload_config(w, world),
         "tflops": tflops,
         "roofline_fraction_layer": roof_time / (ms_step / 1e3) * world,
         "roofline": gate_up_roofline(w, touched, kept, stage_ms["gate_up"], pk, pk_kind, ncu_traffic(w)),
@@ -446,7 +478,7 @@ def main():
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_oracle_rate(w, inp, 15.0)
+        line["cpu_baseline"] = cpu_oracle_rate(w, inp)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

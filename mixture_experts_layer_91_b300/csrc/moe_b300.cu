@@ -493,7 +493,10 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
 // ---------------------------------------------------------------------------
 constexpr int64_t kStaticMaxAssign = MOE_PERMUTE_STATIC_MAX_ASSIGN;
 constexpr int kStaticMaxExperts = 256;
-constexpr int64_t kStaticMaxBlocks = kStaticMaxAssign / kCountBlock;
+// launch_permute runs ceil(T*k / kCountBlock) count blocks; round up the same way
+constexpr int64_t kStaticMaxBlocks = (kStaticMaxAssign + kCountBlock - 1) / kCountBlock;
+static_assert(kStaticMaxBlocks * kCountBlock >= kStaticMaxAssign,
+              "the histogram region must cover every count block of the largest accepted T*k");
 constexpr int64_t kStaticScratchInts = kStaticMaxBlocks * kStaticMaxExperts + kStaticMaxAssign;
 
 // Per-block histograms ([blocks][N_r], blocks <= kStaticMaxBlocks) followed by
@@ -510,7 +513,10 @@ moe_status static_scratch(int32_t** out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_static_scratch[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();   // do not leave the failed lookup as the runtime's last error
+      return MOE_ERR_CUDA;
+    }
     g_static_scratch[dev] = static_cast<int32_t*>(p);
   }
   *out = g_static_scratch[dev];

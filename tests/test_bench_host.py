@@ -63,3 +63,32 @@ def test_kernel_key_ignores_comments_but_not_code():
     assert bench.code_tokens(a) == bench.code_tokens(b)
     assert bench.code_tokens(a) != bench.code_tokens(c)
     assert '"a // b"' in bench.code_tokens(a)        # a // inside a string literal is code
+
+
+def test_reference_arm_reports_what_it_ran(capsys):
+    """--impl reference times the oracle on the fixed sample, step by step:
+    ms_per_step is the measured step time (steps x ms_per_step is the run),
+    value is the sample's tokens over the median step, and its config equals
+    the main arm's."""
+    import argparse
+    import json
+    import time
+
+    w = workloads.TINY_FP32
+    args = argparse.Namespace(steps=2, warmup=1)
+    t0 = time.perf_counter()
+    assert bench.run_reference(args, w) == 0
+    wall = time.perf_counter() - t0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2
+    assert line["ms_per_step"] * line["steps"] / 1e3 <= wall
+    assert line["value"] == pytest.approx(bench.oracle_sample(w).size / (line["ms_per_step"] / 1e3), rel=0.5)
+    assert line["config"] == bench.workload_config(w, 1)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_oracle_sample_is_fixed_and_bounded():
+    w = workloads.DSMOE_16B
+    a, b = bench.oracle_sample(w), bench.oracle_sample(w)
+    assert (a == b).all() and a.size == bench.ORACLE_SAMPLE_TOKENS and len(set(a.tolist())) == a.size
+    assert bench.oracle_sample(workloads.TINY_FP32).size == workloads.TINY_FP32.T
