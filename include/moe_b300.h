@@ -1,5 +1,6 @@
 /*
- * moe_b300.h -- C ABI of the DeepSeekMoE layer forward for one B300 GPU (sm_103a).
+ * moe_b300.h -- C ABI of the DeepSeekMoE layer (forward, and its backward) for one
+ * B300 GPU (sm_103a).
  *
  * The layer (DeepSeekMoE, Chinese translation on gitcode.csdn.net, section 3.2,
  * eqs (9)-(11)):
@@ -308,6 +309,52 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
                                 void* workspace, size_t ws_bytes, void* y,
                                 int32_t* topk_ids_out, float* topk_w_out, int32_t* counts_out,
                                 void* stream, void* const* stage_events);
+
+/* Bytes of scratch moe_backward needs. */
+size_t moe_backward_workspace_size(const moe_config* cfg);
+
+/*
+ * moe_backward -- gradients of the layer for an upstream gradient dy = dL/dy:
+ * dL/dx, dL/dW_g, dL/dW_noise, dL/dW1, dL/dW3, dL/dW2.
+ * The pages define the forward only (DeepSeekMoE translation on
+ * gitcode.csdn.net, section 3.2, eqs (9)-(11); the noisy gate of the
+ * "Mixture of Experts" notes, section 2; GShard's ReLU expert and the expert
+ * capacity, sections 3-4). This is the derivative of that forward with the
+ * top-k selection, and an expert capacity's keep/drop decisions, held fixed
+ * (both are piecewise constant in the inputs): gradients flow through the
+ * selected gates and the kept experts only; a dropped assignment and the
+ * selection bias receive none.
+ *   gate:  dg_{t,j} = <dy_t, FFN_e(u_t)>; renormalised gates pass
+ *          (dg_j - <dg, g>) / sum_sel s to the scores; the softmax of eq (11)
+ *          gives dlogit = s (ds - <ds, s>); the noisy gate gives dH = g (dg -
+ *          <dg, g>) on the kept entries, dlogit = dH, dnoise = dH eps
+ *          sigmoid(x W_noise); dW_g = x^T dlogit, dx += dlogit W_g^T.
+ *   expert (rows X, gate g, a = X W1^T, b = X W3^T, h = silu(a) b):
+ *          dh = dy W2; da = g dh b silu'(a); db = g dh silu(a);
+ *          dX = da W1 + db W3; dW1 = da^T X; dW3 = db^T X; dW2 = (g dy)^T h.
+ *
+ * Arguments are those of moe_forward (the same layer and inputs) plus
+ *   dy        [T, d]          act_dtype   upstream gradient of y
+ *   workspace, ws_bytes                   scratch, >= moe_backward_workspace_size()
+ *   dx        [T, d]          act_dtype (out)
+ *   dW_g      [d, N_r]        fp32 (out)
+ *   dW_noise  [d, N_r]        fp32 (out), required iff gate = NOISY (else ignored)
+ *   dW1, dW3  [K_s+N_r, I, d] fp32 (out) (dW3 may be NULL for ReLU experts)
+ *   dW2       [K_s+N_r, d, I] fp32 (out)
+ * Every output is overwritten (not accumulated into). The call is
+ * self-contained: it recomputes the forward's routing, dispatch and SwiGLU
+ * pre-activations from x (the workspace need not hold a forward's state).
+ * bf16 layers run the expert GEMMs on the tensor cores (bf16 operands: the
+ * saved a, b, g h and the gradient rows da, db, dX are rounded to bf16; fp32
+ * accumulation); fp32 layers run fp32 FMA throughout. The router-weight
+ * gradients are fp32 sums over token chunks combined with fp32 atomics, so
+ * their last bits can vary run to run.
+ */
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
+                        const float* W_noise, const float* eps, const float* bias,
+                        const void* W1, const void* W3, const void* W2, const void* dy,
+                        void* workspace, size_t ws_bytes, void* dx, float* dW_g,
+                        float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream);
 
 /*
  * moe_device_status -- synchronise `stream`, then read and clear the sticky

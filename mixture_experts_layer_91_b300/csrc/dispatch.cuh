@@ -262,7 +262,9 @@ __global__ void __launch_bounds__(256)
 // expert's capacity refused (dest = -1) add nothing. fp32 sums in a fixed
 // order (shared row, then j = 0..k-1), rounded once to bf16. One warp per
 // token; lane j < k holds assignment j's row and gate, each lane sums 8
-// columns (one 16-byte vector) per step. k <= 32.
+// columns (one 16-byte vector) per step. k <= 32. gridDim.y splits the
+// columns into interleaved 256-column slices, so that a small batch (a few
+// tokens of a decode step) still spreads over every SM.
 __global__ void __launch_bounds__(256)
     combine_rows_bf16_kernel(const __nv_bfloat16* __restrict__ O, const int32_t* __restrict__ dest,
                              const int32_t* __restrict__ ids, const float* __restrict__ w,
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(256)
     }
   }
   // the column loop is warp-uniform (the shuffles below need every lane)
-  for (int32_t c0 = 0; c0 < d; c0 += 32 * 8) {
+  for (int32_t c0 = blockIdx.y * 32 * 8; c0 < d; c0 += gridDim.y * 32 * 8) {
     const int32_t c = c0 + lane * 8;
     const bool in = c < d;
     float acc[8];

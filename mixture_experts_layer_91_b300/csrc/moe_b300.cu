@@ -13,8 +13,10 @@
 #include <mutex>
 
 #include "../../include/moe_b300.h"
+#include "backward.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
+#include "gemm_bwd.cuh"
 #include "gemm_simt.cuh"
 #include "gemm_tc.cuh"
 #include "router.cuh"
@@ -24,7 +26,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kVersion = (2 << 16) | 1;
+constexpr int kVersion = (2 << 16) | 2;
 constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
@@ -164,6 +166,53 @@ FwdWs forward_layout(const moe_config* c) {
   return w;
 }
 
+// Backward: the forward's routing and dispatch (recomputed), the saved
+// pre-activations, and the gradient rows. Row spaces as in the forward.
+struct BwdWs {
+  size_t ids, w, counts, offsets, dest, perm_src, blk, rank, mt_start, gsize, a_row, o_row, logits, noise,
+      x_perm, dy_perm, a_pre, b_pre, hg, dg_part, D, rows, dxr, planes, total;
+};
+bool bwd_tc(const moe_config* c) { return c->act_dtype == MOE_DT_BF16; }
+// n-tiles of the dh GEMM, each leaving one partial <dh, h> per row
+int32_t bwd_dg_parts(const moe_config* c) {
+  return bwd_tc(c) ? (c->d_ff + kTcBN - 1) / kTcBN : (c->d_ff + kBsN - 1) / kBsN;
+}
+BwdWs backward_layout(const moe_config* c) {
+  Carver k;
+  BwdWs w;
+  const int64_t n = n_assign(c);
+  const int G = n_groups(c);
+  const int64_t P = padded_rows(c);
+  const size_t ab = act_bytes(c);
+  const int cols = router_cols(c);
+  w.ids = k.take(sizeof(int32_t) * n);
+  w.w = k.take(sizeof(float) * n);
+  w.counts = k.take(sizeof(int32_t) * c->n_routed);
+  w.offsets = k.take(sizeof(int32_t) * (c->n_routed + 1));
+  w.dest = k.take(sizeof(int32_t) * n);
+  w.perm_src = k.take(sizeof(int32_t) * n);
+  w.blk = k.take(sizeof(int32_t) * n_count_blocks(c) * c->n_routed);
+  w.rank = k.take(sizeof(int32_t) * n);
+  w.mt_start = k.take(sizeof(int32_t) * (G + 1));
+  w.gsize = k.take(sizeof(int32_t) * G);
+  w.a_row = k.take(sizeof(int32_t) * G);
+  w.o_row = k.take(sizeof(int32_t) * G);
+  w.logits = k.take(sizeof(float) * c->T * c->n_routed);
+  w.noise = c->gate == MOE_GATE_NOISY ? k.take(sizeof(float) * c->T * c->n_routed) : 0;
+  w.x_perm = k.take(ab * n * c->d);
+  w.dy_perm = k.take(ab * n * c->d);
+  w.a_pre = k.take(ab * P * c->d_ff);
+  w.b_pre = k.take(ab * P * c->d_ff);
+  w.hg = k.take(ab * P * c->d_ff);
+  w.dg_part = k.take(sizeof(float) * P * bwd_dg_parts(c));
+  w.D = k.take(sizeof(float) * c->T * cols);
+  w.rows = k.take(ab * P * c->d);
+  w.dxr = k.take(sizeof(float) * c->T * c->d);
+  w.planes = k.take(router_planes_bytes(c));
+  w.total = k.off;
+  return w;
+}
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -214,6 +263,11 @@ moe_status device_state(DeviceState** out) {
     ok &= cudaFuncSetAttribute(grouped_gemm_tc<kEpiStoreBf16>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(tc_smem_bytes(kEpiStoreBf16))) == cudaSuccess;
+#define MOE_BWD_ATTR(M)                                                                         \
+  ok &= cudaFuncSetAttribute(grouped_gemm_bwd<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                             static_cast<int>(bwd_smem_bytes<M>())) == cudaSuccess;
+    MOE_BWD_ATTR(kBwdSave) MOE_BWD_ATTR(kBwdDH) MOE_BWD_ATTR(kBwdDX) MOE_BWD_ATTR(kBwdWgrad)
+#undef MOE_BWD_ATTR
 #define MOE_RTC_ATTR(NP)                                                                         \
   ok &= cudaFuncSetAttribute(router_tc_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                              static_cast<int>(RtcShape<NP>::smem_bytes)) == cudaSuccess;
@@ -247,6 +301,19 @@ moe_status make_map(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uin
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// 3-D map over [dim2][dim1][dim0] (dim0 contiguous), e.g. a stack of G matrices.
+moe_status make_map_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uint32_t esize, uint64_t d0,
+                       uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[3] = {d0, d1 > 0 ? d1 : 1, d2 > 0 ? d2 : 1};
+  const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 #define MOE_TRY(expr)                   \
@@ -261,9 +328,10 @@ moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : M
 moe_status launch_route(const moe_config* c, const void* x, const float* W_g, const float* W_noise,
                         const float* eps, const float* bias, int32_t* ids, float* w, float* logits,
                         float* zero_rows, int sm_count, void* planes, cudaStream_t st,
-                        const moe_router_stats* stats = nullptr) {
+                        const moe_router_stats* stats = nullptr, float* noise_logits = nullptr) {
   RouterArgs a;
   a.x = x;
+  a.noise_out = noise_logits;
   a.W_g = W_g;
   a.W_noise = W_noise;
   a.eps = eps;
@@ -486,6 +554,136 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     grouped_gemm_simt<kEpiStoreRows><<<grid, kSimtThreads, 0, st>>>(a);
   MOE_TRY(last_launch());
   return mark ? (*mark)(4) : MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// backward: expert GEMMs (tensor cores for bf16 layers, CUDA cores for fp32)
+// ---------------------------------------------------------------------------
+struct BwdPtrs {
+  const void *x, *x_perm, *dy, *dy_perm, *W1, *W3, *W2;
+  const int32_t* perm_src;
+  const float* topk_w;
+  void *a_pre, *b_pre, *hg, *rows;
+  float* dg_part;
+  float *dW1, *dW3, *dW2;
+};
+
+// stage 0: a, b and g*h (recomputed); 1: da, db and the gate partials;
+// 2: the dX rows; 3: the weight gradients
+moe_status launch_bwd_stage(const moe_config* c, const DeviceState* ds, int stage, const GroupPlan& plan,
+                            const BwdPtrs& q, cudaStream_t st) {
+  const int G = n_groups(c);
+  const int64_t P = padded_rows(c);
+  const int I = c->d_ff, d = c->d;
+  const bool relu = c->expert_act == MOE_ACT_RELU;
+  const int64_t n = n_assign(c);
+  if (c->act_dtype != MOE_DT_BF16) {
+    BwdSimtArgs a{};
+    a.plan = plan;
+    a.G = G;
+    a.n_shared = c->n_shared;
+    a.d = d;
+    a.I = I;
+    a.k = c->top_k;
+    a.relu = relu ? 1 : 0;
+    a.x = static_cast<const float*>(q.x);
+    a.x_perm = static_cast<const float*>(q.x_perm);
+    a.dy = static_cast<const float*>(q.dy);
+    a.dy_perm = static_cast<const float*>(q.dy_perm);
+    a.W1 = static_cast<const float*>(q.W1);
+    a.W3 = static_cast<const float*>(q.W3);
+    a.W2 = static_cast<const float*>(q.W2);
+    a.perm_src = q.perm_src;
+    a.topk_w = q.topk_w;
+    a.a_pre = static_cast<float*>(q.a_pre);
+    a.b_pre = static_cast<float*>(q.b_pre);
+    a.hg = static_cast<float*>(q.hg);
+    a.dg_part = q.dg_part;
+    a.dg_stride = bwd_dg_parts(c);
+    a.rows = static_cast<float*>(q.rows);
+    a.dW1 = q.dW1;
+    a.dW3 = q.dW3;
+    a.dW2 = q.dW2;
+    const unsigned grid = static_cast<unsigned>(4 * ds->sm_count);
+    if (stage == 0) bwd_simt<kBwdSave><<<grid, 256, 0, st>>>(a);
+    else if (stage == 1) bwd_simt<kBwdDH><<<grid, 256, 0, st>>>(a);
+    else if (stage == 2) bwd_simt<kBwdDX><<<grid, 256, 0, st>>>(a);
+    else bwd_simt<kBwdWgrad><<<grid, 256, 0, st>>>(a);
+    return last_launch();
+  }
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle s128 = CU_TENSOR_MAP_SWIZZLE_128B, s64 = CU_TENSOR_MAP_SWIZZLE_64B;
+  BwdMaps m{};
+  BwdArgs a{};
+  a.plan = plan;
+  a.G = G;
+  a.n_shared = c->n_shared;
+  a.d = d;
+  a.I = I;
+  a.relu = relu ? 1 : 0;
+  a.perm_src = q.perm_src;
+  a.topk_w = q.topk_w;
+  const unsigned grid = static_cast<unsigned>(ds->sm_count);
+  if (stage == 0) {
+    MOE_TRY(make_map(&m.a[0], q.x, bf, 2, d, c->T, kTcBK, kTcBM, s128));
+    MOE_TRY(make_map(&m.a[1], q.x_perm, bf, 2, d, n, kTcBK, kTcBM, s128));
+    MOE_TRY(make_map(&m.b[0], q.W1, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2, s128));
+    MOE_TRY(make_map(&m.b[1], relu ? q.W1 : q.W3, bf, 2, d, static_cast<uint64_t>(G) * I, kTcBK, kTcBN / 2, s128));
+    MOE_TRY(make_map(&m.out[0], q.a_pre, bf, 2, I, P, 32, 32, s64));
+    MOE_TRY(make_map(&m.out[1], q.b_pre, bf, 2, I, P, 32, 32, s64));
+    MOE_TRY(make_map(&m.out[2], q.hg, bf, 2, I, P, 32, 32, s64));
+    m.a[2] = m.a[3] = m.a[0];
+    m.b[2] = m.b[0];
+    a.n_tiles = relu ? (I + kTcBN - 1) / kTcBN : (I + kTcBN / 2 - 1) / (kTcBN / 2);
+    grouped_gemm_bwd<kBwdSave><<<grid, kTcThreads, bwd_smem_bytes<kBwdSave>(), st>>>(m, a);
+  } else if (stage == 1) {
+    MOE_TRY(make_map(&m.a[0], q.dy, bf, 2, d, c->T, kTcBK, kTcBM, s128));
+    MOE_TRY(make_map(&m.a[1], q.dy_perm, bf, 2, d, n, kTcBK, kTcBM, s128));
+    MOE_TRY(make_map_3d(&m.b[0], q.W2, bf, 2, I, d, G, 64, 64, s128));
+    MOE_TRY(make_map(&m.out[0], q.a_pre, bf, 2, I, P, 32, 32, s64));   // da over a (in place)
+    MOE_TRY(make_map(&m.out[1], q.b_pre, bf, 2, I, P, 32, 32, s64));   // db over b
+    m.a[2] = m.a[3] = m.a[0];
+    m.b[1] = m.b[2] = m.b[0];
+    m.out[2] = m.out[0];
+    a.n_tiles = (I + kTcBN - 1) / kTcBN;
+    a.a_pre = static_cast<const __nv_bfloat16*>(q.a_pre);
+    a.b_pre = static_cast<const __nv_bfloat16*>(q.b_pre);
+    a.dg_part = q.dg_part;
+    grouped_gemm_bwd<kBwdDH><<<grid, kTcThreads, bwd_smem_bytes<kBwdDH>(), st>>>(m, a);
+  } else if (stage == 2) {
+    MOE_TRY(make_map(&m.a[0], q.a_pre, bf, 2, I, P, kTcBK, kTcBM, s128));   // da
+    MOE_TRY(make_map(&m.a[1], q.b_pre, bf, 2, I, P, kTcBK, kTcBM, s128));   // db
+    MOE_TRY(make_map_3d(&m.b[0], q.W1, bf, 2, d, I, G, 64, 64, s128));
+    MOE_TRY(make_map_3d(&m.b[1], relu ? q.W1 : q.W3, bf, 2, d, I, G, 64, 64, s128));
+    MOE_TRY(make_map(&m.out[0], q.rows, bf, 2, d, P, 32, 32, s64));
+    m.a[2] = m.a[3] = m.a[0];
+    m.b[2] = m.b[0];
+    m.out[1] = m.out[2] = m.out[0];
+    a.n_tiles = (d + kTcBN - 1) / kTcBN;
+    // the K_s shared experts have the same rows (dy) and gate 1: one group whose
+    // reduction runs over all of their da, db columns
+    a.fold_mt = c->n_shared > 0 ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
+    grouped_gemm_bwd<kBwdDX><<<grid, kTcThreads, bwd_smem_bytes<kBwdDX>(), st>>>(m, a);
+  } else {
+    MOE_TRY(make_map(&m.a[0], q.a_pre, bf, 2, I, P, 64, 64, s128));      // da
+    MOE_TRY(make_map(&m.a[1], q.b_pre, bf, 2, I, P, 64, 64, s128));      // db
+    MOE_TRY(make_map(&m.a[2], q.dy, bf, 2, d, c->T, 64, 64, s128));
+    MOE_TRY(make_map(&m.a[3], q.dy_perm, bf, 2, d, n, 64, 64, s128));
+    MOE_TRY(make_map(&m.b[0], q.x, bf, 2, d, c->T, 64, 64, s128));
+    MOE_TRY(make_map(&m.b[1], q.x_perm, bf, 2, d, n, 64, 64, s128));
+    MOE_TRY(make_map(&m.b[2], q.hg, bf, 2, I, P, 64, 64, s128));
+    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    MOE_TRY(make_map_3d(&m.out[0], q.dW1, f32, 4, d, I, G, 32, 32, s128));
+    MOE_TRY(make_map_3d(&m.out[1], relu ? q.dW1 : q.dW3, f32, 4, d, I, G, 32, 32, s128));
+    MOE_TRY(make_map_3d(&m.out[2], q.dW2, f32, 4, I, d, G, 32, 32, s128));
+    a.n13 = relu ? 1 : 2;
+    a.mtI = (I + kTcBM - 1) / kTcBM;
+    a.ntD = (d + kTcBN - 1) / kTcBN;
+    a.mtD = (d + kTcBM - 1) / kTcBM;
+    a.ntI = (I + kTcBN - 1) / kTcBN;
+    grouped_gemm_bwd<kBwdWgrad><<<grid, kTcThreads, bwd_smem_bytes<kBwdWgrad>(), st>>>(m, a);
+  }
+  return last_launch();
 }
 
 // ---------------------------------------------------------------------------
@@ -739,7 +937,12 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
   // 4. y_t = shared row + sum_j g_{t,j} row(t, j), one warp per token; or the
   // fp32 accumulator -> bf16 y
   if (by_rows) {
-    const unsigned grid = static_cast<unsigned>((cfg->T + 7) / 8);
+    // one warp per token; with few tokens, the columns are split over CTAs too
+    // (about four CTAs per SM in all)
+    const int64_t tblocks = (cfg->T + 7) / 8;
+    const int64_t slices = (cfg->d + 255) / 256;
+    const int64_t ysplit = std::max<int64_t>(1, std::min<int64_t>(slices, 4ll * ds->sm_count / tblocks));
+    const dim3 grid(static_cast<unsigned>(tblocks), static_cast<unsigned>(ysplit));
     combine_rows_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(rows),
                                                    at<int32_t>(workspace, L.dest), ids, w, po.mt_start,
                                                    po.a_row, cfg->T, cfg->d, cfg->top_k, cfg->n_shared,
@@ -761,6 +964,148 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g, c
                        void* stream) {
   return moe_forward_profiled(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, workspace, ws_bytes, y,
                               topk_ids_out, topk_w_out, counts_out, stream, nullptr);
+}
+
+size_t moe_backward_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return backward_layout(cfg).total;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                        const float* eps, const float* bias, const void* W1, const void* W3, const void* W2,
+                        const void* dy, void* workspace, size_t ws_bytes, void* dx, float* dW_g,
+                        float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const bool noisy = cfg->gate == MOE_GATE_NOISY;
+  const bool swiglu = cfg->expert_act == MOE_ACT_SWIGLU;
+  if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
+  if (W_g == nullptr || W1 == nullptr || (swiglu && W3 == nullptr) || W2 == nullptr || dW_g == nullptr ||
+      dW1 == nullptr || (swiglu && dW3 == nullptr) || dW2 == nullptr || (noisy && dW_noise == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  // with no tokens x, dy, dx, eps and the workspace are not touched
+  if (cfg->T > 0 && (x == nullptr || dy == nullptr || dx == nullptr || workspace == nullptr ||
+                     (noisy && (W_noise == nullptr || eps == nullptr))))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(dy) ||
+      !aligned16(workspace) || !aligned16(dx) || !aligned16(dW1) || !aligned16(dW3) || !aligned16(dW2))
+    return MOE_ERR_INVALID_ARG;
+  const BwdWs L = backward_layout(cfg);
+  if (cfg->T > 0 && ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int E = cfg->n_routed, cols = router_cols(cfg);
+  auto memset0 = [&](void* p, size_t bytes) -> moe_status {
+    if (bytes == 0) return MOE_OK;
+    if (cudaMemsetAsync(p, 0, bytes, st) == cudaSuccess) return MOE_OK;
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  };
+  const int G = n_groups(cfg);
+  MOE_TRY(memset0(dW_g, sizeof(float) * cfg->d * E));
+  if (noisy) MOE_TRY(memset0(dW_noise, sizeof(float) * cfg->d * E));
+  if (cfg->T == 0) {   // no tokens: every gradient is zero
+    MOE_TRY(memset0(dW1, sizeof(float) * G * cfg->d_ff * cfg->d));
+    if (swiglu) MOE_TRY(memset0(dW3, sizeof(float) * G * cfg->d_ff * cfg->d));
+    return memset0(dW2, sizeof(float) * G * cfg->d_ff * cfg->d);
+  }
+  int32_t* ids = at<int32_t>(workspace, L.ids);
+  float* w = at<float>(workspace, L.w);
+  float* logits = at<float>(workspace, L.logits);
+  float* noise = noisy ? at<float>(workspace, L.noise) : nullptr;
+  // 1. the forward's routing, recomputed (logits and noise logits kept)
+  MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w, logits,
+                       nullptr, ds->sm_count, at<void>(workspace, L.planes), st, nullptr, noise));
+  // 2. dispatch and group plan, recomputed; dy gathered into the same row order
+  PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
+             at<int32_t>(workspace, L.a_row), at<int32_t>(workspace, L.o_row)};
+  int32_t* perm_src = at<int32_t>(workspace, L.perm_src);
+  int32_t* dest = at<int32_t>(workspace, L.dest);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  void* x_perm = at<void>(workspace, L.x_perm);
+  void* dy_perm = at<void>(workspace, L.dy_perm);
+  MOE_TRY(launch_permute(cfg, ds, x, ids, at<int32_t>(workspace, L.blk), at<int32_t>(workspace, L.rank),
+                         at<int32_t>(workspace, L.counts), offsets, dest, perm_src, x_perm, &po, st));
+  {
+    const int64_t n = n_assign(cfg);
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 7) / 8, 16ll * ds->sm_count));
+    if (cfg->act_dtype == MOE_DT_BF16)
+      gather_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dy), perm_src,
+                                                              offsets + E, n, cfg->top_k, cfg->d,
+                                                              static_cast<__nv_bfloat16*>(dy_perm),
+                                                              static_cast<__nv_bfloat16*>(x_perm));
+    else
+      gather_rows_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(dy), perm_src, offsets + E, n,
+                                                      cfg->top_k, cfg->d, static_cast<float*>(dy_perm),
+                                                      static_cast<float*>(x_perm));
+    MOE_TRY(last_launch());
+  }
+  GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
+  BwdPtrs q{};
+  q.x = x;
+  q.x_perm = x_perm;
+  q.dy = dy;
+  q.dy_perm = dy_perm;
+  q.W1 = W1;
+  q.W3 = W3;
+  q.W2 = W2;
+  q.perm_src = perm_src;
+  q.topk_w = w;
+  q.a_pre = at<void>(workspace, L.a_pre);
+  q.b_pre = at<void>(workspace, L.b_pre);
+  q.hg = at<void>(workspace, L.hg);
+  q.rows = at<void>(workspace, L.rows);
+  q.dg_part = at<float>(workspace, L.dg_part);
+  q.dW1 = dW1;
+  q.dW3 = dW3;
+  q.dW2 = dW2;
+  // 3. a, b, g*h; then dh = dy W2 with da, db and the gates' partials
+  MOE_TRY(launch_bwd_stage(cfg, ds, 0, gp, q, st));
+  MOE_TRY(launch_bwd_stage(cfg, ds, 1, gp, q, st));
+  // 4. gates -> router logits
+  float* D = at<float>(workspace, L.D);
+  {
+    const unsigned grid = static_cast<unsigned>((cfg->T + 7) / 8);
+    router_bwd_kernel<<<grid, 256, 0, st>>>(logits, noise, noisy ? eps : nullptr, ids, w, dest, q.dg_part,
+                                            bwd_dg_parts(cfg), bwd_dg_parts(cfg), po.mt_start, po.a_row, cfg->T,
+                                            E, cfg->top_k, cfg->n_shared, cfg->renormalize, noisy ? 1 : 0, D,
+                                            nullptr);
+    MOE_TRY(last_launch());
+  }
+  // 5. dX rows of every expert, the router's terms, then the per-token sum
+  MOE_TRY(launch_bwd_stage(cfg, ds, 2, gp, q, st));
+  {
+    const int64_t tchunk = 1024;
+    const dim3 grid(static_cast<unsigned>((cfg->d + kRgTile - 1) / kRgTile),
+                    static_cast<unsigned>((cols + kRgTile - 1) / kRgTile),
+                    static_cast<unsigned>((cfg->T + tchunk - 1) / tchunk));
+    if (cfg->act_dtype == MOE_DT_BF16)
+      router_dw_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), D, cfg->T,
+                                                            cfg->d, E, cols, tchunk, dW_g, dW_noise);
+    else
+      router_dw_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), D, cfg->T, cfg->d, E, cols,
+                                                    tchunk, dW_g, dW_noise);
+    MOE_TRY(last_launch());
+    float* dxr = at<float>(workspace, L.dxr);
+    const dim3 g2(static_cast<unsigned>((cfg->T + kRgTile - 1) / kRgTile),
+                  static_cast<unsigned>((cfg->d + kRgTile - 1) / kRgTile));
+    router_dx_kernel<<<g2, 256, 0, st>>>(D, W_g, noisy ? W_noise : nullptr, cfg->T, cfg->d, E, cols, dxr);
+    MOE_TRY(last_launch());
+    const unsigned g3 = static_cast<unsigned>((cfg->T + 7) / 8);
+    const int32_t fold_mt = static_cast<int32_t>((cfg->T + kTcBM - 1) / kTcBM);
+    if (cfg->act_dtype == MOE_DT_BF16)
+      combine_dx_kernel<__nv_bfloat16, __nv_bfloat16><<<g3, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(q.rows), dest, ids, po.mt_start, po.a_row, dxr, cfg->T, cfg->d,
+          cfg->top_k, cfg->n_shared, cfg->n_shared > 0 ? 1 : 0, fold_mt, static_cast<__nv_bfloat16*>(dx));
+    else
+      combine_dx_kernel<float, float><<<g3, 256, 0, st>>>(static_cast<const float*>(q.rows), dest, ids,
+                                                          po.mt_start, po.a_row, dxr, cfg->T, cfg->d,
+                                                          cfg->top_k, cfg->n_shared, cfg->n_shared, fold_mt,
+                                                          static_cast<float*>(dx));
+    MOE_TRY(last_launch());
+  }
+  // 6. weight gradients: reductions over each expert's rows
+  return launch_bwd_stage(cfg, ds, 3, gp, q, st);
 }
 
 moe_status moe_device_status(void* stream, int32_t* raw) {

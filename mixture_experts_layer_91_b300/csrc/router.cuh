@@ -37,6 +37,7 @@ struct RouterArgs {
   int32_t* topk_ids;     // [T, k]
   float* topk_w;         // [T, k]
   float* logits_out;     // [T, E] or null
+  float* noise_out;      // [T, E] or null: the noise logits x W_noise (noisy gate)
   float* zero_rows;      // [T, zero_width] fp32 rows to clear, or null (the fp32 forward's y)
   int64_t T;
   int32_t d, E, k, renorm, noisy, zero_width;
@@ -418,6 +419,7 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
       }
       if (key[i] != key[i]) key[i] = -INFINITY;   // a NaN key ranks last, ids stay valid
       if (p.logits_out != nullptr && cc < p.E) p.logits_out[t * p.E + cc] = lg[i];
+      if (p.noise_out != nullptr && cc < p.E) p.noise_out[t * p.E + cc] = Lr[p.E + cc];
     }
 
     uint32_t taken = 0;

@@ -291,6 +291,8 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   for (int c = 0; c < NP; ++c) Lrow[c] = acc[c];
   if (p.logits_out != nullptr && valid)
     for (int c = 0; c < E; ++c) p.logits_out[t * E + c] = Lrow[c];
+  if (p.noise_out != nullptr && valid)
+    for (int c = 0; c < E; ++c) p.noise_out[t * E + c] = Lrow[c + E];
 
   // softmax over the E gate logits: max, then the sum of exponentials, each
   // in four interleaved partial chains (element c feeds chain c % 4)

@@ -76,6 +76,13 @@ def _randn_chunked(shape, g, dtype) -> torch.Tensor:
     return out
 
 
+def make_upstream_grad(w: Workload, seed: int) -> torch.Tensor:
+    """dy ~ N(0, 1) [T, d] for a backward pass, stored like x (bf16, or fp32
+    for fp32 workloads), from its own generator."""
+    act = torch.float32 if w.fp32 else torch.bfloat16
+    return torch.randn(w.T, w.d, generator=_gen(seed)).to(act)
+
+
 def random_topk_ids(T: int, n_routed: int, top_k: int, seed: int,
                     skew: str = "uniform") -> torch.Tensor:
     """Valid routing decisions for dispatch tests: k distinct experts per token.
