@@ -280,6 +280,73 @@ def cpu_oracle_rate(w, inp, steps: int = 3) -> dict:
             "kind": "oracle", "sample": oracle_sample_note(w, toks.size, secs)}
 
 
+BWD_STAGES = ["route_dispatch", "save", "dh", "router_bwd", "dx", "router_grads_combine", "wgrad"]
+
+
+def backward_flops(w, kept: int) -> dict:
+    """Algorithmic FLOPs of each backward GEMM stage per launch (`kept` routed
+    rows + K_s T shared rows), one d x I product per weight matrix per row:
+    save (the gate-up recomputed: implementation work, not the derivative's),
+    dh = dy W2, dx = da W1 (+ db W3), wgrad = dW1 (+ dW3) + dW2; and the
+    derivative's own total: twice the forward's expert FLOPs plus the router's
+    two products (x^T dlogit and dlogit W_g^T)."""
+    rows = kept + w.n_shared * w.T
+    unit = 2.0 * rows * w.d * w.d_ff
+    router = 2.0 * w.T * w.d * w.n_routed * (2 if w.noisy else 1)
+    return {"save": (w.n_mats - 1) * unit, "dh": unit, "dx": (w.n_mats - 1) * unit,
+            "wgrad": w.n_mats * unit, "algorithmic": 2 * w.n_mats * unit + 2 * router}
+
+
+def backward_line(args, w, layer, inp, x, eps, stream, barrier, kept: int, pk: dict, pk_kind: str) -> dict:
+    """Time moe_backward (stage events inside the call, on its stream) over
+    the same inputs and a seeded upstream gradient: the layer's backward with
+    the routing recomputed from x (moe_backward is self-contained)."""
+    from mixture_experts_layer_91_b300 import binding
+    dev = x.device
+    dy = inputs.make_upstream_grad(w, seed=w.seed + 500).to(dev)
+    ws = torch.empty(binding.backward_workspace_size(layer.cfg), dtype=torch.uint8, device=dev)
+    call = (layer.cfg, x, layer.W_g, layer.W_noise, eps, layer.bias, layer.W1, layer.W3, layer.W2, dy)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.BWD_PROFILE_EVENTS)]
+          for _ in range(args.steps)]
+    out = binding.backward(*call, workspace=ws, events=ev[0])
+    for _ in range(args.warmup):
+        binding.backward(*call, workspace=ws, out=out, events=ev[0])
+    for e in ev:
+        for x_ in e:
+            x_.record(stream)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        binding.backward(*call, workspace=ws, out=out, events=ev[i])
+    t1.record(stream)
+    barrier()
+    st, raw = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device fault flag {raw} after the backward's timed region")
+    ms = t0.elapsed_time(t1) / args.steps
+    stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, n in enumerate(BWD_STAGES)}
+    fl = backward_flops(w, kept)
+    gemm = {n: fl[n] / (stage_ms[n] / 1e3) / 1e12 for n in ("save", "dh", "dx", "wgrad")}
+    # [W split] + router + count + scan + scatter + gather + save + dh + router bwd + dx
+    # + router dW + router dx + dx sum + wgrad (dW_g cleared by a memset)
+    tc_router = (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
+    launches = 14 + (1 if tc_router else 0)
+    top = max(("save", "dh", "dx", "wgrad"), key=lambda n: stage_ms[n])
+    achieved = gemm[top]
+    return {"ms_per_step": ms, "tokens_per_s": w.T / (ms / 1e3),
+            "tflops": fl["algorithmic"] / (ms / 1e3) / 1e12,
+            "roofline_fraction_layer": fl["algorithmic"] / (pk["bf16_tflops"] * 1e12) / (ms / 1e3),
+            "kernels_ms": stage_ms, "kernels_tflops": gemm, "gpu_launches": launches * args.steps,
+            "roofline": {"bound": "tensor", "kernel": f"grouped_gemm_bwd ({top})", "achieved": achieved,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "peak_kind": f"{pk_kind} burst bf16", "traffic": None,
+                         "algorithmic_flops_per_launch": fl[top]},
+            "outputs": "dx, dW_g, dW1, dW3, dW2 (fp32 weight gradients)" + (", dW_noise" if w.noisy else ""),
+            "note": "self-contained: routing, dispatch and the SwiGLU pre-activations are recomputed from x"}
+
+
 def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
     """Per-step time of the public API over host batches: every step copies its
     x (and eps) in from pinned host memory and its y back out, inside the timed
@@ -361,6 +428,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=None, help="override T (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.BY_NAME[args.workload]
@@ -477,6 +545,10 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if not args.no_backward and not w.fp32:
+        # rank 0 alone (the other ranks have left): a local synchronize, no collective
+        line["backward"] = backward_line(args, w, layer, inp, x, eps, stream, torch.cuda.synchronize, kept, pk,
+                                         pk_kind)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_oracle_rate(w, inp)
     print(json.dumps(line))

@@ -356,6 +356,26 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
                         void* workspace, size_t ws_bytes, void* dx, float* dW_g,
                         float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream);
 
+/* Number of events moe_backward_profiled records per call. */
+#define MOE_BWD_PROFILE_EVENTS 8
+
+/*
+ * moe_backward_profiled -- moe_backward, plus cudaEventRecord of caller-created
+ * events on `stream` at its stage boundaries (stage_events holds
+ * MOE_BWD_PROFILE_EVENTS cudaEvent_t handles, or is NULL: then the call is
+ * moe_backward): [0] start, [1] after the recomputed routing, dispatch and the
+ * gather of dy, [2] after the recomputed a, b, g h, [3] after dh and da, db,
+ * [4] after the router's softmax backward, [5] after the dX rows, [6] after the
+ * router-weight gradient, the router's dx term and the per-token sum, [7] after
+ * the expert weight gradients. With T = 0 no event is recorded.
+ */
+moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const float* W_g,
+                                 const float* W_noise, const float* eps, const float* bias,
+                                 const void* W1, const void* W3, const void* W2, const void* dy,
+                                 void* workspace, size_t ws_bytes, void* dx, float* dW_g,
+                                 float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream,
+                                 void* const* stage_events);
+
 /*
  * moe_device_status -- synchronise `stream`, then read and clear the sticky
  * device fault flag of the current device. Returns MOE_OK,

@@ -34,7 +34,8 @@ EXPORTS = ["moe_status_string", "moe_version", "moe_route_workspace_size", "moe_
            "moe_permute_workspace_size",
            "moe_permute", "moe_permute_static", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_workspace_size", "moe_forward", "moe_forward_profiled", "moe_backward_workspace_size",
-           "moe_backward", "moe_device_status", "moe_debug_wait_timeout"]
+           "moe_backward", "moe_backward_profiled", "moe_device_status", "moe_debug_wait_timeout"]
+BWD_PROFILE_EVENTS = 8   # MOE_BWD_PROFILE_EVENTS
 PROFILE_EVENTS = 6   # MOE_PROFILE_EVENTS
 
 
@@ -97,6 +98,8 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
                                            ctypes.POINTER(P)]),
             "moe_backward_workspace_size": (SZ, [C]),
             "moe_backward": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, P]),
+            "moe_backward_profiled": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, P,
+                                            ctypes.POINTER(P)]),
             "moe_device_status": (I32, [P, ctypes.POINTER(I32)]),
             "moe_debug_wait_timeout": (I32, [ctypes.c_uint32, P]),
         }
@@ -306,11 +309,14 @@ def backward_workspace_size(cfg: MoeConfig) -> int:
     return load().moe_backward_workspace_size(ctypes.byref(cfg))
 
 
-def backward(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, *, workspace=None, stream=None) -> dict:
+def backward(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, *, workspace=None, out=None, events=None,
+             stream=None) -> dict:
     """moe_backward: gradients of the layer for upstream gradient dy.
     Returns a dict dx [T, d] (act dtype), dW_g [d, E], dW_noise [d, E] (noisy
     gate, else None), dW1 / dW3 [G, I, d] (dW3 None for ReLU experts) and
-    dW2 [G, d, I], all fp32 but dx."""
+    dW2 [G, d, I], all fp32 but dx. `out` (a dict like the result) reuses
+    output buffers; `events` (BWD_PROFILE_EVENTS torch.cuda.Event objects)
+    calls moe_backward_profiled, which records them at the stage boundaries."""
     lib = load()
     dt = act_dtype(cfg)
     dev = x.device
@@ -320,21 +326,30 @@ def backward(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, *, workspace=None,
     if workspace is None:
         workspace = _workspace(backward_workspace_size(cfg), dev)
     f32 = torch.float32
-    out = {"dx": torch.empty(cfg.T, d, dtype=dt, device=dev),
+    out = out if out is not None else {"dx": torch.empty(cfg.T, d, dtype=dt, device=dev),
            "dW_g": torch.empty(d, E, dtype=f32, device=dev),
            "dW_noise": torch.empty(d, E, dtype=f32, device=dev) if noisy else None,
            "dW1": torch.empty(G, I, d, dtype=f32, device=dev),
            "dW3": None if relu else torch.empty(G, I, d, dtype=f32, device=dev),
            "dW2": torch.empty(G, d, I, dtype=f32, device=dev)}
-    st = lib.moe_backward(ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(W_g, torch.float32, "W_g"),
-                          _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
-                          _ptr(bias, torch.float32, "bias", True), _ptr(W1, dt, "W1"),
-                          _ptr(W3, dt, "W3", relu), _ptr(W2, dt, "W2"), _ptr(dy, dt, "dy"),
-                          _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), out["dx"].data_ptr(),
-                          out["dW_g"].data_ptr(), _ptr(out["dW_noise"], f32, "dW_noise", True),
-                          out["dW1"].data_ptr(), _ptr(out["dW3"], f32, "dW3", True), out["dW2"].data_ptr(),
-                          _stream(stream))
-    _check(st, "moe_backward")
+    args = [ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(W_g, torch.float32, "W_g"),
+            _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
+            _ptr(bias, torch.float32, "bias", True), _ptr(W1, dt, "W1"),
+            _ptr(W3, dt, "W3", relu), _ptr(W2, dt, "W2"), _ptr(dy, dt, "dy"),
+            _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _ptr(out["dx"], dt, "dx"),
+            _ptr(out["dW_g"], f32, "dW_g"), _ptr(out["dW_noise"], f32, "dW_noise", True),
+            _ptr(out["dW1"], f32, "dW1"), _ptr(out["dW3"], f32, "dW3", True), _ptr(out["dW2"], f32, "dW2"),
+            _stream(stream)]
+    if events is None:
+        _check(lib.moe_backward(*args), "moe_backward")
+        return out
+    if len(events) != BWD_PROFILE_EVENTS:
+        raise ValueError(f"need {BWD_PROFILE_EVENTS} events")
+    for e in events:          # torch creates the CUDA event on first record
+        if e.cuda_event == 0:
+            e.record()
+    arr = (ctypes.c_void_p * BWD_PROFILE_EVENTS)(*[e.cuda_event for e in events])
+    _check(lib.moe_backward_profiled(*args, arr), "moe_backward_profiled")
     return out
 
 

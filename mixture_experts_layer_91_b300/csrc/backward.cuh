@@ -149,27 +149,39 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
-// Router-weight GEMMs (fp32 on the CUDA cores): 64 x 64 output tiles, 256
-// threads with 4 x 4 register tiles, 16-deep K chunks in shared memory.
+// Router-weight GEMMs (fp32 on the CUDA cores): C[m, n] = sum_k A(m, k) B(n, k)
+// over 128 x 128 output tiles, 256 threads with 8 x 8 register tiles, 16-deep
+// K chunks staged k-major in shared memory (float4 reads).
 //   router_dw: dW[c, j] += sum_t x[t, c] D[t, j] over a chunk of tokens
-//              (fp32 atomics across chunks; dW zeroed before)
+//              (M = d, N = cols, K = T; chunks combined with fp32 atomics,
+//              dW zeroed before)
 //   router_dx: dxr[t, c] = sum_j D[t, j] W[c, j], W = [W_g | W_noise]
+//              (M = T, N = d, K = cols)
 // ---------------------------------------------------------------------------
-constexpr int kRgTile = 64, kRgK = 16;
+constexpr int kRgTile = 128, kRgK = 16;
 
-__device__ __forceinline__ void rg_mac(const float (&As)[kRgK][kRgTile + 4], const float (&Bs)[kRgK][kRgTile + 4],
-                                       int ty, int tx, float (&acc)[4][4]) {
+struct RgSmem {
+  float A[kRgK][kRgTile + 4];
+  float B[kRgK][kRgTile + 4];
+};
+
+// Thread (ty, tx) owns tile rows ty*4 .. ty*4+3 and 64+ty*4 .. 64+ty*4+3, and
+// the same pattern of columns with tx.
+__device__ __forceinline__ int rg_idx(int q, int i) { return (i < 4 ? q * 4 : 64 + q * 4 - 4) + i; }
+
+__device__ __forceinline__ void rg_mac(const RgSmem& sm, int ty, int tx, float (&acc)[8][8]) {
 #pragma unroll
   for (int kk = 0; kk < kRgK; ++kk) {
-    float a[4], b[4];
+    const float4 a0 = *reinterpret_cast<const float4*>(&sm.A[kk][ty * 4]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&sm.A[kk][64 + ty * 4]);
+    const float4 b0 = *reinterpret_cast<const float4*>(&sm.B[kk][tx * 4]);
+    const float4 b1 = *reinterpret_cast<const float4*>(&sm.B[kk][64 + tx * 4]);
+    const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
   }
 }
 
@@ -177,28 +189,28 @@ template <typename TX>
 __global__ void __launch_bounds__(256)
     router_dw_kernel(const TX* __restrict__ x, const float* __restrict__ D, int64_t T, int32_t d, int32_t E,
                      int32_t cols, int64_t tchunk, float* __restrict__ dWg, float* __restrict__ dWn) {
-  __shared__ float As[kRgK][kRgTile + 4];
-  __shared__ float Bs[kRgK][kRgTile + 4];
+  __shared__ __align__(16) RgSmem sm;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int32_t m0 = blockIdx.x * kRgTile, n0 = blockIdx.y * kRgTile;
   const int64_t tb = blockIdx.z * tchunk, te = min(T, tb + tchunk);
-  float acc[4][4] = {};
+  float acc[8][8] = {};
   for (int64_t k0 = tb; k0 < te; k0 += kRgK) {
+    // both operands are contiguous along M / N: consecutive threads walk it
     for (int i = tid; i < kRgK * kRgTile; i += 256) {
       const int kk = i / kRgTile, mm = i % kRgTile;
       const int64_t t = k0 + kk;
-      As[kk][mm] = (t < te && m0 + mm < d) ? to_f32(x[t * d + m0 + mm]) : 0.f;
-      Bs[kk][mm] = (t < te && n0 + mm < cols) ? D[t * cols + n0 + mm] : 0.f;
+      sm.A[kk][mm] = (t < te && m0 + mm < d) ? to_f32(x[t * d + m0 + mm]) : 0.f;
+      sm.B[kk][mm] = (t < te && n0 + mm < cols) ? D[t * cols + n0 + mm] : 0.f;
     }
     __syncthreads();
-    rg_mac(As, Bs, ty, tx, acc);
+    rg_mac(sm, ty, tx, acc);
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int32_t c = m0 + ty * 4 + i, jj = n0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int32_t c = m0 + rg_idx(ty, i), jj = n0 + rg_idx(tx, j);
       if (c < d && jj < cols) {
         if (jj < E) atomicAdd(dWg + static_cast<int64_t>(c) * E + jj, acc[i][j]);
         else atomicAdd(dWn + static_cast<int64_t>(c) * E + (jj - E), acc[i][j]);
@@ -209,40 +221,82 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     router_dx_kernel(const float* __restrict__ D, const float* __restrict__ Wg, const float* __restrict__ Wn,
                      int64_t T, int32_t d, int32_t E, int32_t cols, float* __restrict__ dxr) {
-  __shared__ float As[kRgK][kRgTile + 4];
-  __shared__ float Bs[kRgK][kRgTile + 4];
+  __shared__ __align__(16) RgSmem sm;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kRgTile;   // tokens
   const int32_t n0 = blockIdx.y * kRgTile;                          // columns of d
-  float acc[4][4] = {};
+  float acc[8][8] = {};
   for (int k0 = 0; k0 < cols; k0 += kRgK) {
+    // both operands are contiguous along K: consecutive threads walk k
     for (int i = tid; i < kRgK * kRgTile; i += 256) {
-      const int mm = i / kRgK, kk = i % kRgK;   // consecutive threads walk k (contiguous in D and W)
+      const int mm = i / kRgK, kk = i % kRgK;
       const int j = k0 + kk;
-      As[kk][mm] = (m0 + mm < T && j < cols) ? D[(m0 + mm) * cols + j] : 0.f;
+      sm.A[kk][mm] = (m0 + mm < T && j < cols) ? D[(m0 + mm) * cols + j] : 0.f;
       const int32_t c = n0 + mm;
       float wv = 0.f;
       if (c < d && j < cols) wv = j < E ? Wg[static_cast<int64_t>(c) * E + j] : Wn[static_cast<int64_t>(c) * E + (j - E)];
-      Bs[kk][mm] = wv;
+      sm.B[kk][mm] = wv;
     }
     __syncthreads();
-    rg_mac(As, Bs, ty, tx, acc);
+    rg_mac(sm, ty, tx, acc);
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i) {
+    const int64_t t = m0 + rg_idx(ty, i);
+    if (t >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t t = m0 + ty * 4 + i;
-      const int32_t c = n0 + tx * 4 + j;
-      if (t < T && c < d) dxr[t * d + c] = acc[i][j];
+    for (int h = 0; h < 2; ++h) {
+      const int32_t c = n0 + (h ? 64 : 0) + tx * 4;
+      if (c < d)   // d % 8 == 0: four columns are all in or all out
+        *reinterpret_cast<float4*>(dxr + t * d + c) =
+            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
     }
+  }
 }
 
-// dx_t = sum_{s < n_sh} rows[128 * s * fold_mt + t] + sum_j rows[prow(t, j)] + dxr[t]:
-// the shared experts' rows (one folded row, or one per shared expert), the
-// routed experts' rows (their gates were applied to da, db), and the
-// router's term. fp32 sum in a fixed order; one warp per token.
+// eight consecutive elements <-> fp32
+template <typename T>
+struct Vec8;
+template <>
+struct Vec8<__nv_bfloat16> {
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&v)[8]) {
+    uint4 o;
+    o.x = pack_bf16x2(v[0], v[1]);
+    o.y = pack_bf16x2(v[2], v[3]);
+    o.z = pack_bf16x2(v[4], v[5]);
+    o.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = o;
+  }
+};
+template <>
+struct Vec8<float> {
+  __device__ static void load(const float* p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  __device__ static void store(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+
+// dx_t = dxr[t] + sum_{s < n_sh} rows[128 * s * fold_mt + t] + sum_j rows[prow(t, j)]:
+// the router's term, the shared experts' rows (one folded row, or one per
+// shared expert) and the routed experts' rows (their gates were applied to da,
+// db). fp32 sum in a fixed order; one warp per token, eight columns per lane
+// per step (d % 8 == 0); gridDim.y splits the columns when tokens are few.
 template <typename TR, typename TY>
 __global__ void __launch_bounds__(256)
     combine_dx_kernel(const TR* __restrict__ rows, const int32_t* __restrict__ dest,
@@ -251,20 +305,32 @@ __global__ void __launch_bounds__(256)
                       int32_t k, int32_t K_s, int32_t n_sh, int32_t fold_mt, TY* __restrict__ y) {
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
+  if (t >= T) return;   // warp-uniform
   int64_t my_row = -1;
   if (lane < k) {
     const int32_t r = __ldg(dest + t * k + lane);
     if (r >= 0) my_row = assign_prow(r, __ldg(ids + t * k + lane), K_s, mt_start, a_row);
   }
-  for (int32_t c = lane; c < d; c += 32) {
-    float acc = dxr[t * d + c];
-    for (int s = 0; s < n_sh; ++s) acc += to_f32(rows[(128ll * s * fold_mt + t) * d + c]);
+  for (int32_t c0 = blockIdx.y * 256; c0 < d; c0 += gridDim.y * 256) {   // warp-uniform
+    const int32_t c = c0 + lane * 8;
+    const bool in = c < d;
+    float acc[8], v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (in) Vec8<float>::load(dxr + t * d + c, acc);
+    for (int s = 0; s < n_sh && in; ++s) {
+      Vec8<TR>::load(rows + (128ll * s * fold_mt + t) * d + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
     for (int j = 0; j < k; ++j) {
       const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
-      if (row >= 0) acc += to_f32(rows[row * d + c]);
+      if (row < 0 || !in) continue;
+      Vec8<TR>::load(rows + row * d + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
     }
-    y[t * d + c] = from_f32<TY>(acc);
+    if (in) Vec8<TY>::store(y + t * d + c, acc);
   }
 }
 

@@ -388,6 +388,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           gate = c.g < p.n_shared ? 1.f
                                   : __ldg(p.topk_w + __ldg(p.perm_src + __ldg(p.plan.a_row + c.g) + row_local));
       }
+      if (MODE == kBwdDH) {
+        // pull this row's a and b segments of the tile into L2 while the MMAs run
+        const int32_t x0 = c.nt * kTcBN;
+        const int32_t nb = min(kTcBN, p.I - x0) * 2;   // bytes of the segment (I % 8 == 0)
+        const char* pa = reinterpret_cast<const char*>(p.a_pre + prow * p.I + x0);
+        const char* pb = reinterpret_cast<const char*>(p.b_pre + prow * p.I + x0);
+        for (int32_t off = 0; off < nb; off += 128) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(pa + off));
+          if (!p.relu) asm volatile("prefetch.global.L2 [%0];" ::"l"(pb + off));
+        }
+      }
       if (!mbar_wait(bar_tfull + 8 * b, aph, abort)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kTcBN;
@@ -445,8 +456,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int v = 0; v < 4; ++v) {
             uint4 ua = make_uint4(0u, 0u, 0u, 0u), ub = ua;
             if (x + 8 * v < p.I) {   // I % 8 == 0: a 16-byte vector is all in or all out
-              ua = *reinterpret_cast<const uint4*>(arow + x + 8 * v);
-              if (!p.relu) ub = *reinterpret_cast<const uint4*>(brow + x + 8 * v);
+              ua = __ldg(reinterpret_cast<const uint4*>(arow + x + 8 * v));
+              if (!p.relu) ub = __ldg(reinterpret_cast<const uint4*>(brow + x + 8 * v));
             }
             av[4 * v] = ua.x; av[4 * v + 1] = ua.y; av[4 * v + 2] = ua.z; av[4 * v + 3] = ua.w;
             bv[4 * v] = ub.x; bv[4 * v + 1] = ub.y; bv[4 * v + 2] = ub.z; bv[4 * v + 3] = ub.w;

@@ -441,8 +441,8 @@ moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void
           c->d, dest, perm_src, static_cast<__nv_bfloat16*>(x_perm));
     else
       scatter_kernel<float><<<grid, 256, 0, st>>>(ids, n, c->top_k, E, blk, rank, offsets, c->capacity,
-                                                  static_cast<const float*>(x), c->d, dest,
-                                                  perm_src, static_cast<float*>(x_perm));
+                                                        static_cast<const float*>(x), c->d, dest,
+                                                        perm_src, static_cast<float*>(x_perm));
     MOE_TRY(last_launch());
   }
   return MOE_OK;
@@ -971,10 +971,11 @@ size_t moe_backward_workspace_size(const moe_config* cfg) {
   return backward_layout(cfg).total;
 }
 
-moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
-                        const float* eps, const float* bias, const void* W1, const void* W3, const void* W2,
-                        const void* dy, void* workspace, size_t ws_bytes, void* dx, float* dW_g,
-                        float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream) {
+moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                                 const float* eps, const float* bias, const void* W1, const void* W3,
+                                 const void* W2, const void* dy, void* workspace, size_t ws_bytes, void* dx,
+                                 float* dW_g, float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream,
+                                 void* const* stage_events) {
   MOE_TRY(check_config(cfg));
   const bool noisy = cfg->gate == MOE_GATE_NOISY;
   const bool swiglu = cfg->expert_act == MOE_ACT_SWIGLU;
@@ -995,6 +996,13 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, 
   MOE_TRY(device_state(&ds));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int E = cfg->n_routed, cols = router_cols(cfg);
+  auto mark = [&](int i) -> moe_status {
+    if (stage_events == nullptr) return MOE_OK;
+    if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st) == cudaSuccess) return MOE_OK;
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  };
   auto memset0 = [&](void* p, size_t bytes) -> moe_status {
     if (bytes == 0) return MOE_OK;
     if (cudaMemsetAsync(p, 0, bytes, st) == cudaSuccess) return MOE_OK;
@@ -1009,6 +1017,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, 
     if (swiglu) MOE_TRY(memset0(dW3, sizeof(float) * G * cfg->d_ff * cfg->d));
     return memset0(dW2, sizeof(float) * G * cfg->d_ff * cfg->d);
   }
+  MOE_TRY(mark(0));
   int32_t* ids = at<int32_t>(workspace, L.ids);
   float* w = at<float>(workspace, L.w);
   float* logits = at<float>(workspace, L.logits);
@@ -1059,9 +1068,12 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, 
   q.dW1 = dW1;
   q.dW3 = dW3;
   q.dW2 = dW2;
+  MOE_TRY(mark(1));
   // 3. a, b, g*h; then dh = dy W2 with da, db and the gates' partials
   MOE_TRY(launch_bwd_stage(cfg, ds, 0, gp, q, st));
+  MOE_TRY(mark(2));
   MOE_TRY(launch_bwd_stage(cfg, ds, 1, gp, q, st));
+  MOE_TRY(mark(3));
   // 4. gates -> router logits
   float* D = at<float>(workspace, L.D);
   {
@@ -1072,10 +1084,15 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, 
                                             nullptr);
     MOE_TRY(last_launch());
   }
+  MOE_TRY(mark(4));
   // 5. dX rows of every expert, the router's terms, then the per-token sum
   MOE_TRY(launch_bwd_stage(cfg, ds, 2, gp, q, st));
+  MOE_TRY(mark(5));
   {
-    const int64_t tchunk = 1024;
+    // split the token reduction so that about two CTAs per SM stream x and D
+    const int64_t tiles = ((cfg->d + kRgTile - 1) / kRgTile) * ((cols + kRgTile - 1) / kRgTile);
+    const int64_t nchunk = std::max<int64_t>(1, std::min<int64_t>((cfg->T + 255) / 256, 2ll * ds->sm_count / tiles));
+    const int64_t tchunk = (cfg->T + nchunk - 1) / nchunk;
     const dim3 grid(static_cast<unsigned>((cfg->d + kRgTile - 1) / kRgTile),
                     static_cast<unsigned>((cols + kRgTile - 1) / kRgTile),
                     static_cast<unsigned>((cfg->T + tchunk - 1) / tchunk));
@@ -1091,7 +1108,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, 
                   static_cast<unsigned>((cfg->d + kRgTile - 1) / kRgTile));
     router_dx_kernel<<<g2, 256, 0, st>>>(D, W_g, noisy ? W_noise : nullptr, cfg->T, cfg->d, E, cols, dxr);
     MOE_TRY(last_launch());
-    const unsigned g3 = static_cast<unsigned>((cfg->T + 7) / 8);
+    const int64_t tblocks = (cfg->T + 7) / 8;
+    const int64_t ysplit = std::max<int64_t>(1, std::min<int64_t>((cfg->d + 255) / 256, 4ll * ds->sm_count / tblocks));
+    const dim3 g3(static_cast<unsigned>(tblocks), static_cast<unsigned>(ysplit));
     const int32_t fold_mt = static_cast<int32_t>((cfg->T + kTcBM - 1) / kTcBM);
     if (cfg->act_dtype == MOE_DT_BF16)
       combine_dx_kernel<__nv_bfloat16, __nv_bfloat16><<<g3, 256, 0, st>>>(
@@ -1104,8 +1123,18 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, 
                                                           static_cast<float*>(dx));
     MOE_TRY(last_launch());
   }
+  MOE_TRY(mark(6));
   // 6. weight gradients: reductions over each expert's rows
-  return launch_bwd_stage(cfg, ds, 3, gp, q, st);
+  MOE_TRY(launch_bwd_stage(cfg, ds, 3, gp, q, st));
+  return mark(7);
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                        const float* eps, const float* bias, const void* W1, const void* W3, const void* W2,
+                        const void* dy, void* workspace, size_t ws_bytes, void* dx, float* dW_g,
+                        float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream) {
+  return moe_backward_profiled(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, workspace, ws_bytes, dx, dW_g,
+                               dW_noise, dW1, dW3, dW2, stream, nullptr);
 }
 
 moe_status moe_device_status(void* stream, int32_t* raw) {

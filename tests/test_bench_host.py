@@ -92,3 +92,16 @@ def test_oracle_sample_is_fixed_and_bounded():
     a, b = bench.oracle_sample(w), bench.oracle_sample(w)
     assert (a == b).all() and a.size == bench.ORACLE_SAMPLE_TOKENS and len(set(a.tolist())) == a.size
     assert bench.oracle_sample(workloads.TINY_FP32).size == workloads.TINY_FP32.T
+
+
+def test_backward_flops_count_each_weight_product_twice():
+    """The derivative's own FLOPs are twice the forward's expert FLOPs (dgrad +
+    wgrad) plus the router's two products; the recomputed gate-up is counted
+    per stage but not in the algorithmic total."""
+    for w in (workloads.DSMOE_16B, workloads.GSHARD_RELU_CAP):
+        kept = w.T * w.top_k
+        fl = bench.backward_flops(w, kept)
+        fwd = bench.kernel_flops(w, kept)
+        assert fl["save"] == pytest.approx(fwd["gate_up"])
+        assert fl["dh"] + fl["dx"] + fl["wgrad"] == pytest.approx(2 * (fwd["gate_up"] + fwd["down"]))
+        assert fl["algorithmic"] == pytest.approx(2 * (fwd["gate_up"] + fwd["down"]) + 2 * fwd["router"])
