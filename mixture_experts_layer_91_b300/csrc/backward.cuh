@@ -18,6 +18,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "dispatch.cuh"
 #include "gemm_bwd.cuh"
 #include "gemm_tc.cuh"
 
@@ -63,22 +64,49 @@ __device__ __forceinline__ int64_t assign_prow(int32_t dest, int32_t e, int32_t 
   return 128ll * __ldg(mt_start + g) + (dest - __ldg(a_row + g));
 }
 
+// Where the router's gradient rows go: fp32 D [T, cols] (fp32 layers), or
+// (bf16 layers, for the tensor-core GEMMs of the router's terms) three bf16
+// planes of [rows, Ep] each: P0 = hi = bf16(v), P1 = lo = bf16(v - hi),
+// P2 = hi again; columns [cols, Ep) and rows [T, rows) are zero.
+struct RouterGradOut {
+  float* D;
+  __nv_bfloat16* planes;
+  int64_t plane_rows;
+  int32_t Ep;
+};
+
 // Gates -> router logits, one warp per token (k <= 32, E <= 256). L and Nl
 // are the logits x W_g and (noisy gate) the noise logits x W_noise, [T, E].
-// Writes D [T, cols]: d logit in columns [0, E), d noise logit in [E, 2E)
-// (noisy). dg of assignment j is the sum of its n-tile partials <dh, h> (0
-// when an expert's capacity dropped it: it added nothing to y).
+// Writes the rows of D [T, cols]: d logit in columns [0, E), d noise logit in
+// [E, 2E) (noisy). dg of assignment j is the sum of its n-tile partials
+// <dh, h> (0 when an expert's capacity dropped it: it added nothing to y).
 __global__ void __launch_bounds__(256)
     router_bwd_kernel(const float* __restrict__ L, const float* __restrict__ Nl, const float* __restrict__ eps,
                       const int32_t* __restrict__ ids, const float* __restrict__ w,
                       const int32_t* __restrict__ dest, const float* __restrict__ dg_part, int32_t dg_stride,
                       int32_t dg_parts, const int32_t* __restrict__ mt_start, const int32_t* __restrict__ a_row,
                       int64_t T, int32_t E, int32_t k, int32_t K_s, int32_t renorm, int32_t noisy,
-                      float* __restrict__ D, float* __restrict__ dg_out) {
+                      RouterGradOut out, float* __restrict__ dg_out) {
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;   // warp-uniform
   const int cols = noisy ? 2 * E : E;
+  auto put = [&](int col, float v) {
+    if (out.planes == nullptr) {
+      out.D[t * cols + col] = v;
+      return;
+    }
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    const int64_t r = t * out.Ep + col, pl = out.plane_rows * out.Ep;
+    out.planes[r] = hi;
+    out.planes[pl + r] = lo;
+    out.planes[2 * pl + r] = hi;
+  };
+  if (out.planes != nullptr) {   // zero padding: columns past cols, rows past T
+    if (t >= out.plane_rows) return;
+    for (int col = (t < T ? cols : 0) + lane; col < out.Ep; col += 32) put(col, 0.f);
+  }
+  if (t >= T) return;   // warp-uniform
   const float* Lr = L + t * E;
   int32_t id = -1;
   float g = 0.f, dg = 0.f;
@@ -97,7 +125,6 @@ __global__ void __launch_bounds__(256)
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
   };
-  float* Dr = D + t * cols;
   if (noisy) {
     const float c = wsum(dg * g);
     const float dH = g * (dg - c);   // softmax over the kept H
@@ -116,7 +143,7 @@ __global__ void __launch_bounds__(256)
           }
         }
       }
-      Dr[col] = v;
+      put(col, v);
     }
     return;
   }
@@ -144,7 +171,7 @@ __global__ void __launch_bounds__(256)
       const float dsj = __shfl_sync(0xffffffffu, ds, j);
       if (idj == col) dsc = dsj;
     }
-    Dr[col] = expf(Lr[col] - m) * inv * (dsc - dot);
+    put(col, expf(Lr[col] - m) * inv * (dsc - dot));
   }
 }
 
@@ -252,6 +279,74 @@ __global__ void __launch_bounds__(256)
         *reinterpret_cast<float4*>(dxr + t * d + c) =
             make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
     }
+  }
+}
+
+// The router terms of the bf16 backward on the tensor cores:
+//   dxr = D W^T     = P0 Wh^T + P1 Wh^T + P2 Wl^T (forward grouped GEMM, fp32
+//                     rows, the three plane pairs folded along K like the
+//                     shared experts), W = Wh + Wl, P0 + P1 = D to ~2^-17;
+//   dW  = x^T D     = x^T P0 + x^T P1 (weight-gradient GEMM over token chunks,
+//                     each chunk and plane one group), partials summed below.
+// router_wplanes_kernel: Wp [3][d][Ep] bf16 = (Wh, Wh, Wl) of W = [W_g | W_noise]
+// (columns past cols zero).
+__global__ void router_wplanes_kernel(const float* __restrict__ Wg, const float* __restrict__ Wn, int32_t d,
+                                      int32_t E, int32_t cols, int32_t Ep, __nv_bfloat16* __restrict__ Wp) {
+  const int64_t n = static_cast<int64_t>(d) * Ep;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t c = i / Ep;
+    const int32_t j = static_cast<int32_t>(i % Ep);
+    float v = 0.f;
+    if (j < cols) v = j < E ? Wg[c * E + j] : Wn[c * E + (j - E)];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    Wp[i] = hi;
+    Wp[n + i] = hi;
+    Wp[2 * n + i] = lo;
+  }
+}
+
+// Group plans of the two router GEMMs (one CTA). dx plan: three groups of T
+// rows at planes 0, 1, 2 (mt_start 0, f, 2f, 3f with f = plane_rows / 128),
+// output rows 0 (the fold puts all three into group 0). dW plan: 2 nc groups,
+// token chunk c of plane p (0 = hi, 1 = lo): A rows (x) from c * chunk, B rows
+// (planes) from p * plane_rows + c * chunk.
+__global__ void router_plans_kernel(int64_t T, int64_t plane_rows, int32_t nc, int32_t chunk, PlanOut dxp,
+                                    PlanOut dwp) {
+  const int32_t f = static_cast<int32_t>(plane_rows / 128);
+  for (int g = threadIdx.x; g < 4; g += blockDim.x) {
+    dxp.mt_start[g] = g * f;
+    if (g < 3) {
+      dxp.gsize[g] = static_cast<int32_t>(T);
+      dxp.a_row[g] = 0;
+      dxp.o_row[g] = 0;
+    }
+  }
+  for (int g = threadIdx.x; g < 2 * nc; g += blockDim.x) {
+    const int32_t c = g % nc, pl = g / nc;
+    const int64_t r0 = static_cast<int64_t>(c) * chunk;
+    const int64_t left = T - r0;
+    dwp.gsize[g] = static_cast<int32_t>(left <= 0 ? 0 : (left < chunk ? left : chunk));
+    dwp.a_row[g] = static_cast<int32_t>(r0);
+    dwp.mt_start[g] = static_cast<int32_t>((pl * plane_rows + r0) / 128);
+    dwp.o_row[g] = 0;
+  }
+}
+
+// dW_g[c, j] (j < E) and dW_noise[c, j - E] (j in [E, cols)) = sum over the
+// groups of the partials [groups][d][Ep], in a fixed order.
+__global__ void router_dw_reduce_kernel(const float* __restrict__ part, int32_t groups, int32_t d, int32_t E,
+                                        int32_t cols, int32_t Ep, float* __restrict__ dWg, float* __restrict__ dWn) {
+  const int64_t n = static_cast<int64_t>(d) * cols;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t c = i / cols;
+    const int32_t j = static_cast<int32_t>(i % cols);
+    float acc = 0.f;
+    for (int g = 0; g < groups; ++g) acc += part[(static_cast<int64_t>(g) * d + c) * Ep + j];
+    if (j < E) dWg[c * E + j] = acc;
+    else dWn[c * E + (j - E)] = acc;
   }
 }
 

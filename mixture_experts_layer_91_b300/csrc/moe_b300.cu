@@ -170,8 +170,22 @@ FwdWs forward_layout(const moe_config* c) {
 // pre-activations, and the gradient rows. Row spaces as in the forward.
 struct BwdWs {
   size_t ids, w, counts, offsets, dest, perm_src, blk, rank, mt_start, gsize, a_row, o_row, logits, noise,
-      x_perm, dy_perm, a_pre, b_pre, hg, dg_part, D, rows, dxr, planes, total;
+      x_perm, dy_perm, a_pre, b_pre, hg, dg_part, D, rows, dxr, planes;
+  // bf16 layers: the router terms on the tensor cores (gradient planes, weight
+  // planes, chunk partials of dW, and the two GEMMs' group plans)
+  size_t gplanes, wplanes, wpart, plan_dx, plan_dw, total;
 };
+// Router terms of the bf16 backward: router columns padded to whole 64-wide
+// k-blocks, token rows to whole 128-row tiles, and the token chunks of dW.
+int32_t rg_ep(const moe_config* c) { return (router_cols(c) + 63) / 64 * 64; }
+int64_t rg_rows(const moe_config* c) { return (c->T + 127) / 128 * 128; }
+int32_t rg_chunks(const moe_config* c) {
+  return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(16, (c->T + 1023) / 1024)));
+}
+int32_t rg_chunk_rows(const moe_config* c) {
+  const int64_t nc = rg_chunks(c);
+  return static_cast<int32_t>(((c->T + nc - 1) / nc + 127) / 128 * 128);
+}
 bool bwd_tc(const moe_config* c) { return c->act_dtype == MOE_DT_BF16; }
 // n-tiles of the dh GEMM, each leaving one partial <dh, h> per row
 int32_t bwd_dg_parts(const moe_config* c) {
@@ -205,10 +219,17 @@ BwdWs backward_layout(const moe_config* c) {
   w.b_pre = k.take(ab * P * c->d_ff);
   w.hg = k.take(ab * P * c->d_ff);
   w.dg_part = k.take(sizeof(float) * P * bwd_dg_parts(c));
-  w.D = k.take(sizeof(float) * c->T * cols);
+  w.D = bwd_tc(c) ? 0 : k.take(sizeof(float) * c->T * cols);
   w.rows = k.take(ab * P * c->d);
   w.dxr = k.take(sizeof(float) * c->T * c->d);
   w.planes = k.take(router_planes_bytes(c));
+  const bool tc = bwd_tc(c);
+  const int nc = rg_chunks(c);
+  w.gplanes = tc ? k.take(sizeof(__nv_bfloat16) * 3 * rg_rows(c) * rg_ep(c)) : 0;
+  w.wplanes = tc ? k.take(sizeof(__nv_bfloat16) * 3 * c->d * rg_ep(c)) : 0;
+  w.wpart = tc ? k.take(sizeof(float) * 2 * nc * c->d * rg_ep(c)) : 0;
+  w.plan_dx = tc ? k.take(sizeof(int32_t) * 4 * 4) : 0;
+  w.plan_dw = tc ? k.take(sizeof(int32_t) * 4 * (2 * nc + 1)) : 0;
   w.total = k.off;
   return w;
 }
@@ -686,6 +707,84 @@ moe_status launch_bwd_stage(const moe_config* c, const DeviceState* ds, int stag
   return last_launch();
 }
 
+// The router's two gradient products of a bf16 layer on the tensor cores
+// (the gradient planes are written by router_bwd_kernel):
+//   dxr [T, d] fp32 = P0 Wh^T + P1 Wh^T + P2 Wl^T, through the forward grouped
+//     GEMM's fp32-row epilogue with the three plane pairs as folded groups;
+//   dW = x^T (P0 + P1) over token chunks through the weight-gradient GEMM,
+//     each (chunk, plane) a group with its own fp32 partial, then summed.
+moe_status launch_router_terms_tc(const moe_config* c, const DeviceState* ds, const void* x, const float* W_g,
+                                  const float* W_noise, const __nv_bfloat16* gplanes, void* workspace,
+                                  const BwdWs& L, float* dxr, float* dW_g, float* dW_noise, cudaStream_t st) {
+  const int E = c->n_routed, cols = router_cols(c), d = c->d;
+  const int32_t Ep = rg_ep(c);
+  const int64_t prow = rg_rows(c);
+  const int32_t nc = rg_chunks(c), chunk = rg_chunk_rows(c);
+  __nv_bfloat16* wplanes = at<__nv_bfloat16>(workspace, L.wplanes);
+  float* wpart = at<float>(workspace, L.wpart);
+  int32_t* pdx = at<int32_t>(workspace, L.plan_dx);
+  int32_t* pdw = at<int32_t>(workspace, L.plan_dw);
+  const int gw = 2 * nc;
+  PlanOut dxp{pdx, pdx + 4, pdx + 8, pdx + 12};
+  PlanOut dwp{pdw, pdw + (gw + 1), pdw + 2 * (gw + 1), pdw + 3 * (gw + 1)};
+  {
+    const int64_t n = static_cast<int64_t>(d) * Ep;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4ll * ds->sm_count));
+    router_wplanes_kernel<<<grid, 256, 0, st>>>(W_g, W_noise, d, E, cols, Ep, wplanes);
+    MOE_TRY(last_launch());
+    router_plans_kernel<<<1, 64, 0, st>>>(c->T, prow, nc, chunk, dxp, dwp);
+    MOE_TRY(last_launch());
+  }
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle s128 = CU_TENSOR_MAP_SWIZZLE_128B;
+  const unsigned grid = static_cast<unsigned>(ds->sm_count);
+  {
+    TcMaps m{};
+    MOE_TRY(make_map(&m.a0, gplanes, bf, 2, Ep, 3 * prow, kTcBK, kTcBM, s128));
+    MOE_TRY(make_map(&m.b0, wplanes, bf, 2, Ep, 3ll * d, kTcBK, kTcBN, s128));
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    m.out = m.a0;
+    TcArgs a{};
+    a.plan = GroupPlan{dxp.mt_start, dxp.gsize, dxp.a_row, dxp.o_row};
+    a.G = 3;
+    a.n_shared = 3;
+    a.K = Ep;
+    a.n_tiles = (d + kTcBN - 1) / kTcBN;
+    a.b_rows = d;
+    a.n_out = d;
+    a.out = dxr;
+    a.top_k = 1;
+    a.fold_mt = static_cast<int32_t>(prow / kTcBM);
+    grouped_gemm_tc<kEpiStoreRows><<<grid, kTcThreads, tc_smem_bytes(kEpiStoreRows), st>>>(m, a);
+    MOE_TRY(last_launch());
+  }
+  {
+    BwdMaps m{};
+    MOE_TRY(make_map(&m.a[3], x, bf, 2, d, c->T, 64, 64, s128));
+    MOE_TRY(make_map(&m.b[2], gplanes, bf, 2, Ep, 3 * prow, 64, 64, s128));
+    MOE_TRY(make_map_3d(&m.out[2], wpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Ep, d, gw, 32, 32, s128));
+    m.a[0] = m.a[1] = m.a[2] = m.a[3];
+    m.b[0] = m.b[1] = m.b[2];
+    m.out[0] = m.out[1] = m.out[2];
+    BwdArgs a{};
+    a.plan = GroupPlan{dwp.mt_start, dwp.gsize, dwp.a_row, dwp.o_row};
+    a.G = gw;
+    a.n_shared = 0;
+    a.d = d;
+    a.I = Ep;
+    a.n13 = 0;
+    a.mtD = (d + kTcBM - 1) / kTcBM;
+    a.ntI = (Ep + kTcBN - 1) / kTcBN;
+    grouped_gemm_bwd<kBwdWgrad><<<grid, kTcThreads, bwd_smem_bytes<kBwdWgrad>(), st>>>(m, a);
+    MOE_TRY(last_launch());
+  }
+  const int64_t n = static_cast<int64_t>(d) * cols;
+  router_dw_reduce_kernel<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4ll * ds->sm_count)), 256, 0,
+                            st>>>(wpart, gw, d, E, cols, Ep, dW_g, dW_noise);
+  return last_launch();
+}
+
 // ---------------------------------------------------------------------------
 // fixed scratch of moe_permute_static (no caller workspace, no allocation)
 // ---------------------------------------------------------------------------
@@ -1074,13 +1173,18 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
   MOE_TRY(mark(2));
   MOE_TRY(launch_bwd_stage(cfg, ds, 1, gp, q, st));
   MOE_TRY(mark(3));
-  // 4. gates -> router logits
-  float* D = at<float>(workspace, L.D);
+  // 4. gates -> router logits (fp32 rows, or bf16 hi/lo planes for the tensor cores)
+  const bool tc = bwd_tc(cfg);
+  float* D = tc ? nullptr : at<float>(workspace, L.D);
+  __nv_bfloat16* gplanes = tc ? at<__nv_bfloat16>(workspace, L.gplanes) : nullptr;
+  const int32_t Ep = rg_ep(cfg);
+  const int64_t prow = rg_rows(cfg);
   {
-    const unsigned grid = static_cast<unsigned>((cfg->T + 7) / 8);
+    RouterGradOut ro{D, gplanes, prow, Ep};
+    const unsigned grid = static_cast<unsigned>(((tc ? prow : cfg->T) + 7) / 8);
     router_bwd_kernel<<<grid, 256, 0, st>>>(logits, noise, noisy ? eps : nullptr, ids, w, dest, q.dg_part,
                                             bwd_dg_parts(cfg), bwd_dg_parts(cfg), po.mt_start, po.a_row, cfg->T,
-                                            E, cfg->top_k, cfg->n_shared, cfg->renormalize, noisy ? 1 : 0, D,
+                                            E, cfg->top_k, cfg->n_shared, cfg->renormalize, noisy ? 1 : 0, ro,
                                             nullptr);
     MOE_TRY(last_launch());
   }
@@ -1088,7 +1192,11 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
   // 5. dX rows of every expert, the router's terms, then the per-token sum
   MOE_TRY(launch_bwd_stage(cfg, ds, 2, gp, q, st));
   MOE_TRY(mark(5));
-  {
+  float* dxr = at<float>(workspace, L.dxr);
+  if (tc) {
+    MOE_TRY(launch_router_terms_tc(cfg, ds, x, W_g, noisy ? W_noise : nullptr, gplanes, workspace, L, dxr, dW_g,
+                                   noisy ? dW_noise : nullptr, st));
+  } else {
     // split the token reduction so that about two CTAs per SM stream x and D
     const int64_t tiles = ((cfg->d + kRgTile - 1) / kRgTile) * ((cols + kRgTile - 1) / kRgTile);
     const int64_t nchunk = std::max<int64_t>(1, std::min<int64_t>((cfg->T + 255) / 256, 2ll * ds->sm_count / tiles));
@@ -1103,11 +1211,12 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
       router_dw_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), D, cfg->T, cfg->d, E, cols,
                                                     tchunk, dW_g, dW_noise);
     MOE_TRY(last_launch());
-    float* dxr = at<float>(workspace, L.dxr);
     const dim3 g2(static_cast<unsigned>((cfg->T + kRgTile - 1) / kRgTile),
                   static_cast<unsigned>((cfg->d + kRgTile - 1) / kRgTile));
     router_dx_kernel<<<g2, 256, 0, st>>>(D, W_g, noisy ? W_noise : nullptr, cfg->T, cfg->d, E, cols, dxr);
     MOE_TRY(last_launch());
+  }
+  {
     const int64_t tblocks = (cfg->T + 7) / 8;
     const int64_t ysplit = std::max<int64_t>(1, std::min<int64_t>((cfg->d + 255) / 256, 4ll * ds->sm_count / tblocks));
     const dim3 g3(static_cast<unsigned>(tblocks), static_cast<unsigned>(ysplit));
