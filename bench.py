@@ -353,14 +353,15 @@ def e2e_ms(args, layer, inp, x, eps, stream, barrier, world, dev) -> float:
     region; the copies of neighbouring steps overlap the forward
     (MoELayer.forward_host_stream)."""
     n = args.steps
-    x_hosts = [inp["x"].pin_memory() for _ in range(2)]
-    eps_hosts = [inp["eps"].pin_memory() for _ in range(2)] if inp["eps"] is not None else None
-    y_hosts = [torch.empty(tuple(layer.y.shape), dtype=layer.y.dtype, pin_memory=True) for _ in range(2)]
+    nb = 3   # host batches in rotation (as many as the pipeline's device buffers)
+    x_hosts = [inp["x"].pin_memory() for _ in range(nb)]
+    eps_hosts = [inp["eps"].pin_memory() for _ in range(nb)] if inp["eps"] is not None else None
+    y_hosts = [torch.empty(tuple(layer.y.shape), dtype=layer.y.dtype, pin_memory=True) for _ in range(nb)]
 
     def run(k):
-        xs = [x_hosts[i & 1] for i in range(k)]
-        es = [eps_hosts[i & 1] for i in range(k)] if eps_hosts is not None else None
-        return layer.forward_host_stream(xs, [y_hosts[i & 1] for i in range(k)], es)
+        xs = [x_hosts[i % nb] for i in range(k)]
+        es = [eps_hosts[i % nb] for i in range(k)] if eps_hosts is not None else None
+        return layer.forward_host_stream(xs, [y_hosts[i % nb] for i in range(k)], es, depth=nb)
 
     run(max(args.warmup, 2))
     barrier()

@@ -396,45 +396,49 @@ class MoELayer:
         return forward_profiled(self.cfg, x, self.W_g, self.W_noise, eps, self.bias, self.W1, self.W3,
                                 self.W2, workspace=self.workspace, y=self.y, events=events)
 
-    def forward_host_stream(self, x_hosts, y_hosts, eps_hosts=None):
+    def forward_host_stream(self, x_hosts, y_hosts, eps_hosts=None, depth: int = 3):
         """Run the layer over a sequence of batches held in pinned host memory.
 
         Batch i is copied in on an upload stream, computed on the current
-        stream and copied back into y_hosts[i] on a download stream, with two
-        device buffers for x and y, so the copies of batches i+1 and i-1
-        overlap the forward of batch i. Every copy is enqueued before this
-        returns; synchronise the current stream (or the returned event) to
-        read y_hosts. Returns the CUDA event recorded after the last copy-back.
+        stream and copied back into y_hosts[i] on a download stream, through
+        `depth` device buffers for x and y, so the copies of the next and the
+        previous batches overlap the forward of batch i (and a copy never
+        waits for the buffer of the step just before). Every copy is enqueued
+        before this returns; synchronise the current stream (or the returned
+        event) to read y_hosts. Returns the CUDA event recorded after the last
+        copy-back.
         """
         n = len(x_hosts)
         if len(y_hosts) != n or (eps_hosts is not None and len(eps_hosts) != n):
             raise ValueError("one output (and eps) buffer per input batch")
+        if depth < 2:
+            raise ValueError("depth >= 2")
         comp = torch.cuda.current_stream(self.device)
         up = self._streams.setdefault("up", torch.cuda.Stream(self.device))
         down = self._streams.setdefault("down", torch.cuda.Stream(self.device))
-        if "x" not in self._bufs:
-            self._bufs["x"] = [torch.empty_like(x_hosts[0], device=self.device) for _ in range(2)]
-            self._bufs["y"] = [torch.empty_like(self.y) for _ in range(2)]
+        if len(self._bufs.get("x", [])) != depth or (eps_hosts is not None and "eps" not in self._bufs):
+            self._bufs["x"] = [torch.empty_like(x_hosts[0], device=self.device) for _ in range(depth)]
+            self._bufs["y"] = [torch.empty_like(self.y) for _ in range(depth)]
             if eps_hosts is not None:
-                self._bufs["eps"] = [torch.empty_like(eps_hosts[0], device=self.device) for _ in range(2)]
+                self._bufs["eps"] = [torch.empty_like(eps_hosts[0], device=self.device) for _ in range(depth)]
         xb, yb, eb = self._bufs["x"], self._bufs["y"], self._bufs.get("eps")
-        uploaded = [torch.cuda.Event() for _ in range(2)]
-        computed = [torch.cuda.Event() for _ in range(2)]
-        downloaded = [torch.cuda.Event() for _ in range(2)]
+        uploaded = [torch.cuda.Event() for _ in range(depth)]
+        computed = [torch.cuda.Event() for _ in range(depth)]
+        downloaded = [torch.cuda.Event() for _ in range(depth)]
         up.wait_stream(comp)      # buffers may still be read by earlier work on `comp`
         down.wait_stream(comp)
         for i in range(n):
-            b = i & 1
+            b = i % depth
             with torch.cuda.stream(up):
-                if i >= 2:
-                    up.wait_event(computed[b])          # forward i-2 has read xb[b]
+                if i >= depth:
+                    up.wait_event(computed[b])          # forward i-depth has read xb[b]
                 xb[b].copy_(x_hosts[i], non_blocking=True)
                 if eb is not None:
                     eb[b].copy_(eps_hosts[i], non_blocking=True)
                 uploaded[b].record(up)
             comp.wait_event(uploaded[b])
-            if i >= 2:
-                comp.wait_event(downloaded[b])          # copy-back i-2 has read yb[b]
+            if i >= depth:
+                comp.wait_event(downloaded[b])          # copy-back i-depth has read yb[b]
             self(xb[b], eb[b] if eb is not None else None, y=yb[b])
             computed[b].record(comp)
             with torch.cuda.stream(down):

@@ -360,7 +360,8 @@ def test_forward_is_repeatable(cuda_lib):
     assert (y1 - y2).abs().max().item() <= 1e-2 * y1.abs().max().item()
 
 
-def test_host_stream_matches_device_forward(cuda_lib):
+@pytest.mark.parametrize("depth", [2, 3])
+def test_host_stream_matches_device_forward(depth, cuda_lib):
     """Overlapped host-batch pipeline: each y equals the device forward of its x."""
     w = workloads.GSHARD_NOISY.with_tokens(512)
     inp = get_inputs(w)
@@ -369,7 +370,7 @@ def test_host_stream_matches_device_forward(cuda_lib):
     xs = [torch.randn(w.T, w.d, generator=g).to(torch.bfloat16).pin_memory() for _ in range(5)]
     es = [torch.randn(w.T, w.n_routed, generator=g).pin_memory() for _ in range(5)]
     ys = [torch.empty(w.T, w.d, dtype=torch.bfloat16, pin_memory=True) for _ in range(5)]
-    layer.forward_host_stream(xs, ys, es)
+    layer.forward_host_stream(xs, ys, es, depth=depth)
     torch.cuda.synchronize()
     for i in range(5):
         ref = layer(xs[i].to(DEV), es[i].to(DEV)).float().cpu().numpy()
