@@ -79,6 +79,18 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
+// One TMA load of a whole MN-major tile: the tensor viewed as [outer][MN / 64]
+// [K rows][64] (4-D; 3-D without the outer index), so a box of {64, 64, n, 1}
+// lands as n consecutive 8 KB boxes, the layout the descriptor expects.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                            int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
 struct BwdMaps {
   // kBwdSave : a0 x, a1 x_perm; b0 W1, b1 W3 (or W1 again for ReLU) [G*I, d] box 64x128;
   //            out0 a, out1 b, out2 g*h [P, I] bf16 32x32 boxes
@@ -106,6 +118,10 @@ struct BwdArgs {
   float* dg_part;           // DH: per-row partial <dh, h> of each n-tile [P, n_tiles]
   // weight-gradient tile space per group: n13 jobs of (mtI x ntD) tiles (dW1, dW3), then mtD x ntI (dW2)
   int32_t n13, mtI, ntD, mtD, ntI;
+  // 1: the MN-major operands' maps are chunked views (one TMA load per tile:
+  // 4-D for the weights of DH / DX, 3-D for the row operands of the weight
+  // gradients); 0: one 2-D / 3-D box of 64 per 8 KB
+  int32_t packed;
 };
 
 // operand ring + two staging boxes per epilogue warp + barriers (fp32 wgrad
@@ -273,9 +289,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_2d(sb + kTileBBytes / 2, &maps.b[1], full, kb * kTcBK, b_y + (p.relu ? kTcBN / 2 : 0));
           } else if (MODE == kBwdDH) {
             tma_load_2d(sa, amap, full, kb * kTcBK, a_y);
+            if (p.packed) {
+              tma_load_4d(sb, &maps.b[0], full, 0, kb * kTcBK, c.nt * 4, c.g);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_3d(sb + j * kMnBoxBytes, &maps.b[0], full, c.nt * kTcBN + 64 * j, kb * kTcBK, c.g);
+              for (int j = 0; j < 4; ++j)
+                tma_load_3d(sb + j * kMnBoxBytes, &maps.b[0], full, c.nt * kTcBN + 64 * j, kb * kTcBK, c.g);
+            }
           } else if (MODE == kBwdDX) {
             // k-block kb: expert e (folded shared group) / half h (da W1 or db W3) / block kx
             const int32_t e = kb / (halves * nk_base);
@@ -284,9 +304,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int32_t kx = r - h * nk_base;
             tma_load_2d(sa, &maps.a[h], full, kx * kTcBK, a_y + e * p.fold_mt * kTcBM);
             const int32_t gz = fused ? e : c.g;
+            if (p.packed) {
+              tma_load_4d(sb, &maps.b[h], full, 0, kx * kTcBK, c.nt * 4, gz);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_3d(sb + j * kMnBoxBytes, &maps.b[h], full, c.nt * kTcBN + 64 * j, kx * kTcBK, gz);
+              for (int j = 0; j < 4; ++j)
+                tma_load_3d(sb + j * kMnBoxBytes, &maps.b[h], full, c.nt * kTcBN + 64 * j, kx * kTcBK, gz);
+            }
+          } else if (p.packed) {
+            tma_load_3d(sa, amap, full, 0, a_y + kb * kTcBK, c.mt * 2);
+            tma_load_3d(sb, bmap, full, 0, b_y + kb * kTcBK, c.nt * 4);
           } else {
 #pragma unroll
             for (int j = 0; j < 2; ++j)

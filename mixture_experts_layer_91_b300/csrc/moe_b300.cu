@@ -335,6 +335,24 @@ moe_status make_map_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, 
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// A bf16 matrix of `rows` rows and `cols` (a multiple of 64) contiguous columns,
+// row pitch `pitch` elements, viewed as [outer][cols / 64][rows][64] (outer =
+// 1: 3-D) with the 128-byte swizzle: a box {64, 64, chunks(, 1)} is `chunks`
+// consecutive 64 x 64 MN-major boxes in one TMA load. `outer_stride` (elements)
+// separates the stacked matrices.
+moe_status make_map_chunked(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t pitch,
+                            uint64_t outer, uint64_t outer_stride, uint32_t chunks) {
+  const bool four = outer > 1;
+  const cuuint64_t dims[4] = {64, rows > 0 ? rows : 1, cols / 64, outer};
+  const cuuint64_t strides[3] = {pitch * 2, 128, outer_stride * 2};
+  const cuuint32_t box[4] = {64, 64, chunks, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, four ? 4 : 3, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 #define MOE_TRY(expr)                   \
@@ -660,7 +678,12 @@ moe_status launch_bwd_stage(const moe_config* c, const DeviceState* ds, int stag
   } else if (stage == 1) {
     MOE_TRY(make_map(&m.a[0], q.dy, bf, 2, d, c->T, kTcBK, kTcBM, s128));
     MOE_TRY(make_map(&m.a[1], q.dy_perm, bf, 2, d, n, kTcBK, kTcBM, s128));
-    MOE_TRY(make_map_3d(&m.b[0], q.W2, bf, 2, I, d, G, 64, 64, s128));
+    // W2 [G][d][I]: one load per 256-wide tile where I is a multiple of 64
+    a.packed = I % 64 == 0 ? 1 : 0;
+    if (a.packed)
+      MOE_TRY(make_map_chunked(&m.b[0], q.W2, d, I, I, G, static_cast<uint64_t>(d) * I, 4));
+    else
+      MOE_TRY(make_map_3d(&m.b[0], q.W2, bf, 2, I, d, G, 64, 64, s128));
     MOE_TRY(make_map(&m.out[0], q.a_pre, bf, 2, I, P, 32, 32, s64));   // da over a (in place)
     MOE_TRY(make_map(&m.out[1], q.b_pre, bf, 2, I, P, 32, 32, s64));   // db over b
     m.a[2] = m.a[3] = m.a[0];
@@ -674,8 +697,15 @@ moe_status launch_bwd_stage(const moe_config* c, const DeviceState* ds, int stag
   } else if (stage == 2) {
     MOE_TRY(make_map(&m.a[0], q.a_pre, bf, 2, I, P, kTcBK, kTcBM, s128));   // da
     MOE_TRY(make_map(&m.a[1], q.b_pre, bf, 2, I, P, kTcBK, kTcBM, s128));   // db
-    MOE_TRY(make_map_3d(&m.b[0], q.W1, bf, 2, d, I, G, 64, 64, s128));
-    MOE_TRY(make_map_3d(&m.b[1], relu ? q.W1 : q.W3, bf, 2, d, I, G, 64, 64, s128));
+    // W1, W3 [G][I][d]: one load per 256-wide tile where d is a multiple of 64
+    a.packed = d % 64 == 0 ? 1 : 0;
+    if (a.packed) {
+      MOE_TRY(make_map_chunked(&m.b[0], q.W1, I, d, d, G, static_cast<uint64_t>(I) * d, 4));
+      MOE_TRY(make_map_chunked(&m.b[1], relu ? q.W1 : q.W3, I, d, d, G, static_cast<uint64_t>(I) * d, 4));
+    } else {
+      MOE_TRY(make_map_3d(&m.b[0], q.W1, bf, 2, d, I, G, 64, 64, s128));
+      MOE_TRY(make_map_3d(&m.b[1], relu ? q.W1 : q.W3, bf, 2, d, I, G, 64, 64, s128));
+    }
     MOE_TRY(make_map(&m.out[0], q.rows, bf, 2, d, P, 32, 32, s64));
     m.a[2] = m.a[3] = m.a[0];
     m.b[2] = m.b[0];
@@ -686,13 +716,25 @@ moe_status launch_bwd_stage(const moe_config* c, const DeviceState* ds, int stag
     a.fold_mt = c->n_shared > 0 ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
     grouped_gemm_bwd<kBwdDX><<<grid, kTcThreads, bwd_smem_bytes<kBwdDX>(), st>>>(m, a);
   } else {
-    MOE_TRY(make_map(&m.a[0], q.a_pre, bf, 2, I, P, 64, 64, s128));      // da
-    MOE_TRY(make_map(&m.a[1], q.b_pre, bf, 2, I, P, 64, 64, s128));      // db
-    MOE_TRY(make_map(&m.a[2], q.dy, bf, 2, d, c->T, 64, 64, s128));
-    MOE_TRY(make_map(&m.a[3], q.dy_perm, bf, 2, d, n, 64, 64, s128));
-    MOE_TRY(make_map(&m.b[0], q.x, bf, 2, d, c->T, 64, 64, s128));
-    MOE_TRY(make_map(&m.b[1], q.x_perm, bf, 2, d, n, 64, 64, s128));
-    MOE_TRY(make_map(&m.b[2], q.hg, bf, 2, I, P, 64, 64, s128));
+    // row operands: one load per tile (2 chunks of A, 4 of B) where I and d are multiples of 64
+    a.packed = (I % 64 == 0 && d % 64 == 0) ? 1 : 0;
+    if (a.packed) {
+      MOE_TRY(make_map_chunked(&m.a[0], q.a_pre, P, I, I, 1, 0, 2));     // da
+      MOE_TRY(make_map_chunked(&m.a[1], q.b_pre, P, I, I, 1, 0, 2));     // db
+      MOE_TRY(make_map_chunked(&m.a[2], q.dy, c->T, d, d, 1, 0, 2));
+      MOE_TRY(make_map_chunked(&m.a[3], q.dy_perm, n, d, d, 1, 0, 2));
+      MOE_TRY(make_map_chunked(&m.b[0], q.x, c->T, d, d, 1, 0, 4));
+      MOE_TRY(make_map_chunked(&m.b[1], q.x_perm, n, d, d, 1, 0, 4));
+      MOE_TRY(make_map_chunked(&m.b[2], q.hg, P, I, I, 1, 0, 4));
+    } else {
+      MOE_TRY(make_map(&m.a[0], q.a_pre, bf, 2, I, P, 64, 64, s128));      // da
+      MOE_TRY(make_map(&m.a[1], q.b_pre, bf, 2, I, P, 64, 64, s128));      // db
+      MOE_TRY(make_map(&m.a[2], q.dy, bf, 2, d, c->T, 64, 64, s128));
+      MOE_TRY(make_map(&m.a[3], q.dy_perm, bf, 2, d, n, 64, 64, s128));
+      MOE_TRY(make_map(&m.b[0], q.x, bf, 2, d, c->T, 64, 64, s128));
+      MOE_TRY(make_map(&m.b[1], q.x_perm, bf, 2, d, n, 64, 64, s128));
+      MOE_TRY(make_map(&m.b[2], q.hg, bf, 2, I, P, 64, 64, s128));
+    }
     const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     MOE_TRY(make_map_3d(&m.out[0], q.dW1, f32, 4, d, I, G, 32, 32, s128));
     MOE_TRY(make_map_3d(&m.out[1], relu ? q.dW1 : q.dW3, f32, 4, d, I, G, 32, 32, s128));
