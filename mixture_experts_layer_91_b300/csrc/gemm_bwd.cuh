@@ -124,13 +124,22 @@ struct BwdArgs {
   int32_t packed;
 };
 
-// operand ring + two staging boxes per epilogue warp + barriers (fp32 wgrad
-// boxes: 1024 + 4 x 48 KB + 32 KB + 256 = 225.25 KB, inside the 227 KB limit)
+// Epilogue staging per warp: two 32 x 32 boxes (double-buffered stores; fp32
+// boxes for the weight gradients), or for DH two sets of an a box and a b box
+// (loads of the saved a, b, overwritten in place by da, db and stored from there).
+__host__ __device__ constexpr uint32_t bwd_staging_bytes(int m) {
+  return kTcEpiWarps * (m == kBwdDH ? 4u : 2u) * bwd_box_bytes(m);
+}
+constexpr uint32_t kBwdBarBytes = 512;   // stage / accumulator / epilogue-load mbarriers, TMEM slot, abort flag
+
+// operand ring + staging + barriers: at most 1024 + 4 x 48 KB + 32 KB + 512 =
+// 225.5 KB, inside the 227 KB limit
 template <int MODE>
 constexpr size_t bwd_smem_bytes() {
-  return 1024 + static_cast<size_t>(kTcStages) * kStageBytes + kTcEpiWarps * 2 * bwd_box_bytes(MODE) + 256;
+  return 1024 + static_cast<size_t>(kTcStages) * kStageBytes + bwd_staging_bytes(MODE) + kBwdBarBytes;
 }
 static_assert(bwd_smem_bytes<kBwdWgrad>() <= 227 * 1024, "shared memory of the weight-gradient kernel");
+static_assert(bwd_smem_bytes<kBwdDH>() <= 227 * 1024, "shared memory of the dh kernel");
 
 struct BwdTile {
   int32_t g, lmt, mt, nt;
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + kTileABytes;
   const uint32_t sStore = base + kTcStages * kStageBytes;
-  const uint32_t sBar = sStore + kTcEpiWarps * 2 * kBox;
+  const uint32_t sBar = sStore + bwd_staging_bytes(MODE);
   uint8_t* gBar = gbase + (sBar - base);
   const uint32_t bar_full = sBar;
   const uint32_t bar_empty = sBar + 8 * kTcStages;
@@ -198,6 +207,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_drain = bar_tempty + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gBar + 16 * kTcStages + 40);
   volatile int* abort = reinterpret_cast<volatile int*>(gBar + 16 * kTcStages + 44);
+  const uint32_t bar_epi = sBar + 16 * kTcStages + 64;   // DH: two a/b load barriers per epilogue warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -212,6 +222,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar_tempty + 8 * b, kTcEpiWarps);
     }
     mbar_init(bar_drain, 1);
+    if (MODE == kBwdDH)
+      for (int i = 0; i < 2 * kTcEpiWarps; ++i) mbar_init(bar_epi + 8 * i, 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -377,6 +389,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;
     const uint32_t buf0 = sStore + ew * 2 * kBox;
     uint32_t local = 0, nstore = 0;
+    // DH: this warp's two sets [a box | b box], their load barriers and phases
+    const uint32_t dh_sets = sStore + ew * 4 * kBox;
+    const uint32_t dh_bar = bar_epi + 16 * ew;
+    uint32_t dh_ph[2] = {0u, 0u};    // loads waited for, per set
+    uint32_t dh_iss[2] = {0u, 0u};   // loads issued, per set (lane 0)
+    auto dh_issue = [&](int32_t x, int32_t y, uint32_t set) {   // lane 0
+      const uint32_t buf = dh_sets + set * 2 * kBox;
+      const uint32_t bar = dh_bar + 8 * set;
+      ++dh_iss[set];
+      mbar_arrive_expect_tx(bar, (p.relu ? 1u : 2u) * kBox);
+      tma_load_2d(buf, &maps.out[0], bar, x, y);                       // a (da is stored over it)
+      if (!p.relu) tma_load_2d(buf + kBox, &maps.out[1], bar, x, y);   // b (db)
+    };
 
     // stage one 32 x 32 box (this warp's 32 rows) and TMA-store it
     auto store_box_bf16 = [&](const uint32_t (&hp)[16], const CUtensorMap* map, int32_t x, int32_t y) {
@@ -415,16 +440,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           gate = c.g < p.n_shared ? 1.f
                                   : __ldg(p.topk_w + __ldg(p.perm_src + __ldg(p.plan.a_row + c.g) + row_local));
       }
-      if (MODE == kBwdDH) {
-        // pull this row's a and b segments of the tile into L2 while the MMAs run
-        const int32_t x0 = c.nt * kTcBN;
-        const int32_t nb = min(kTcBN, p.I - x0) * 2;   // bytes of the segment (I % 8 == 0)
-        const char* pa = reinterpret_cast<const char*>(p.a_pre + prow * p.I + x0);
-        const char* pb = reinterpret_cast<const char*>(p.b_pre + prow * p.I + x0);
-        for (int32_t off = 0; off < nb; off += 128) {
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(pa + off));
-          if (!p.relu) asm volatile("prefetch.global.L2 [%0];" ::"l"(pb + off));
-        }
+      if (MODE == kBwdDH && lane == 0) {
+        // the tile's first two chunks of a and b, loaded while its MMAs run (the
+        // previous tile's stores must have read both sets first)
+        bulk_wait_read<0>();
+        const int32_t x0 = c.nt * kTcBN, nchunk = (min(kTcBN, p.I - x0) + 31) / 32;
+        for (int cc = 0; cc < 2 && cc < nchunk; ++cc) dh_issue(x0 + 32 * cc, c.mt * kTcBM + q * 32, cc);
       }
       if (!mbar_wait(bar_tfull + 8 * b, aph, abort)) break;
       tc_fence_after();
@@ -468,26 +489,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           store_box_bf16(hp, &maps.out[2], x, y);
         }
       } else if (MODE == kBwdDH) {
-        // acc = dh (unscaled) for 256 columns of I; a, b read back from the saved rows
+        // acc = dh (unscaled) for 256 columns of I. a and b arrive in the
+        // warp's two sets of 32 x 32 boxes (64-byte swizzle: 16-byte chunk j of
+        // row r at chunk j ^ ((r >> 1) & 3)); da and db are written over them
+        // and stored from there; chunk cc + 2 is loaded into a set once chunk
+        // cc's stores have read it.
         float dgp = 0.f;
-        const __nv_bfloat16* arow = p.a_pre + prow * p.I;
-        const __nv_bfloat16* brow = p.b_pre + prow * p.I;
+        const int32_t x0 = c.nt * kTcBN, nchunk = (min(kTcBN, p.I - x0) + 31) / 32;
+        const int32_t y = c.mt * kTcBM + q * 32;
+        bool ok_ld = true;
 #pragma unroll 1
-        for (int cc = 0; cc < kTcBN / 32; ++cc) {
-          const int32_t x = c.nt * kTcBN + cc * 32;
-          if (x >= p.I) break;   // warp-uniform
+        for (int cc = 0; cc < nchunk; ++cc) {
+          const uint32_t set = static_cast<uint32_t>(cc) & 1u;
+          const uint32_t abuf = dh_sets + set * 2 * kBox, bbuf = abuf + kBox;
           uint32_t dh[32];
           tmem_ld_32x32b_x32(tacc + cc * 32, dh);
+          ok_ld = __all_sync(0xffffffffu, ok_ld && mbar_wait(dh_bar + 8 * set, dh_ph[set] & 1u, abort));
+          ++dh_ph[set];
           uint32_t av[16], bv[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 ua = make_uint4(0u, 0u, 0u, 0u), ub = ua;
-            if (x + 8 * v < p.I) {   // I % 8 == 0: a 16-byte vector is all in or all out
-              ua = __ldg(reinterpret_cast<const uint4*>(arow + x + 8 * v));
-              if (!p.relu) ub = __ldg(reinterpret_cast<const uint4*>(brow + x + 8 * v));
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(av[4 * j]), "=r"(av[4 * j + 1]), "=r"(av[4 * j + 2]), "=r"(av[4 * j + 3])
+                         : "r"(abuf + off)
+                         : "memory");
+            if (!p.relu) {
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(bv[4 * j]), "=r"(bv[4 * j + 1]), "=r"(bv[4 * j + 2]), "=r"(bv[4 * j + 3])
+                           : "r"(bbuf + off)
+                           : "memory");
+            } else {
+              bv[4 * j] = bv[4 * j + 1] = bv[4 * j + 2] = bv[4 * j + 3] = 0u;
             }
-            av[4 * v] = ua.x; av[4 * v + 1] = ua.y; av[4 * v + 2] = ua.z; av[4 * v + 3] = ua.w;
-            bv[4 * v] = ub.x; bv[4 * v + 1] = ub.y; bv[4 * v + 2] = ub.z; bv[4 * v + 3] = ub.w;
           }
           tmem_ld_wait();
           uint32_t dap[16], dbp[16];
@@ -516,9 +550,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dap[j] = pack_bf16x2(da2[0], da2[1]);
             dbp[j] = pack_bf16x2(db2[0], db2[1]);
           }
-          const int32_t y = c.mt * kTcBM + q * 32;
-          store_box_bf16(dap, &maps.out[0], x, y);
-          if (!p.relu) store_box_bf16(dbp, &maps.out[1], x, y);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(abuf + off), "r"(dap[4 * j]),
+                         "r"(dap[4 * j + 1]), "r"(dap[4 * j + 2]), "r"(dap[4 * j + 3])
+                         : "memory");
+            if (!p.relu)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bbuf + off), "r"(dbp[4 * j]),
+                           "r"(dbp[4 * j + 1]), "r"(dbp[4 * j + 2]), "r"(dbp[4 * j + 3])
+                           : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.out[0], abuf, x0 + 32 * cc, y);
+            if (!p.relu) tma_store_2d(&maps.out[1], bbuf, x0 + 32 * cc, y);
+            bulk_commit();
+            if (cc + 2 < nchunk) {   // reuse this set for chunk cc + 2 once its stores have read it
+              bulk_wait_read<0>();
+              dh_issue(x0 + 32 * (cc + 2), y, set);
+            }
+          }
+          __syncwarp();
         }
         if (row_local < __ldg(p.plan.gsize + c.g)) p.dg_part[prow * p.n_tiles + c.nt] = dgp;
       } else if (MODE == kBwdDX) {
@@ -578,6 +632,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
     }
     if (lane == 0) bulk_wait<0>();
+    if (MODE == kBwdDH && lane == 0) {
+      // after an abort, loads this warp issued may not have been waited for:
+      // they must land before the CTA exits
+      for (uint32_t set = 0; set < 2; ++set)
+        for (; dh_ph[set] < dh_iss[set]; ++dh_ph[set]) {
+          volatile int never = 0;
+          mbar_wait(dh_bar + 8 * set, dh_ph[set] & 1u, &never, 100000000ull);
+        }
+    }
   }
 
   __syncthreads();
