@@ -327,8 +327,35 @@ def backward_line(args, w, layer, inp, x, eps, stream, barrier, kept: int, pk: d
         raise RuntimeError(f"device fault flag {raw} after the backward's timed region")
     ms = t0.elapsed_time(t1) / args.steps
     stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, n in enumerate(BWD_STAGES)}
+    # a training step without the recompute: moe_forward_train (y, and the
+    # backward's state in the workspace) then moe_backward_from_forward
+    y_t = torch.empty_like(layer.y)
+    fw = (layer.cfg, x, layer.W_g, layer.W_noise, eps, layer.bias, layer.W1, layer.W3, layer.W2)
+    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        binding.forward_train(*fw, workspace=ws, y=y_t)
+        binding.backward(*fw, dy, workspace=ws, out=out, from_forward=True)
+    barrier()
+    for i in range(args.steps):
+        tev[i][0].record(stream)
+        binding.forward_train(*fw, workspace=ws, y=y_t)
+        tev[i][1].record(stream)
+        binding.backward(*fw, dy, workspace=ws, out=out, from_forward=True)
+        tev[i][2].record(stream)
+    barrier()
+    st, raw = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device fault flag {raw} after the training steps")
+    f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in tev)
+    b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in tev)
     fl = backward_flops(w, kept)
     gemm = {n: fl[n] / (stage_ms[n] / 1e3) / 1e12 for n in ("save", "dh", "dx", "wgrad")}
+    fwd_flops = sum(kernel_flops(w, kept).values())
+    train = {"ms_per_step": f_ms + b_ms, "forward_train_ms": f_ms, "backward_from_forward_ms": b_ms,
+             "tokens_per_s": w.T / ((f_ms + b_ms) / 1e3),
+             "tflops": (fwd_flops + fl["algorithmic"]) / ((f_ms + b_ms) / 1e3) / 1e12,
+             "note": "moe_forward_train + moe_backward_from_forward: the backward reuses the forward's routing, "
+                     "dispatch and saved a, b, g h"}
     # [W split] + router + count + scan + scatter + gather + save + dh + router bwd + dx
     # + router dW + router dx + dx sum + wgrad (dW_g cleared by a memset)
     tc_router = (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
@@ -343,6 +370,7 @@ def backward_line(args, w, layer, inp, x, eps, stream, barrier, kept: int, pk: d
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                          "peak_kind": f"{pk_kind} burst bf16", "traffic": None,
                          "algorithmic_flops_per_launch": fl[top]},
+            "train_step": train,
             "outputs": "dx, dW_g, dW1, dW3, dW2 (fp32 weight gradients)" + (", dW_noise" if w.noisy else ""),
             "note": "self-contained: routing, dispatch and the SwiGLU pre-activations are recomputed from x"}
 

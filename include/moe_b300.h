@@ -377,6 +377,37 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
                                  void* const* stage_events);
 
 /*
+ * moe_forward_train -- the forward of a training step: moe_forward's y, plus
+ * the state the backward needs, left in `workspace` (>=
+ * moe_backward_workspace_size()): the routing, the logits (and noise logits),
+ * the dispatch and group plan, x_perm, and the expert pre-activations a, b and
+ * g * h. y is formed from g * h through W2 and the per-token sum of the rows
+ * (the gates ride on g * h), so it is the sum of moe_forward; bf16 layers use
+ * the row combine whatever cfg->combine says, fp32 layers the scatter-add.
+ * Arguments as in moe_forward.
+ */
+moe_status moe_forward_train(const moe_config* cfg, const void* x, const float* W_g,
+                             const float* W_noise, const float* eps, const float* bias,
+                             const void* W1, const void* W3, const void* W2,
+                             void* workspace, size_t ws_bytes, void* y, void* stream);
+
+/*
+ * moe_backward_from_forward -- moe_backward (same arguments, results and
+ * precision) on a workspace that moe_forward_train filled for the same cfg,
+ * x, router weights, noise, bias and expert weights, with nothing in between
+ * that wrote to it: the routing, the dispatch and the recompute of a, b and
+ * g * h are skipped. It consumes the state (da and db overwrite the saved a
+ * and b in place): call it once per moe_forward_train. stage_events: as in
+ * moe_backward_profiled, or NULL.
+ */
+moe_status moe_backward_from_forward(const moe_config* cfg, const void* x, const float* W_g,
+                                     const float* W_noise, const float* eps, const float* bias,
+                                     const void* W1, const void* W3, const void* W2, const void* dy,
+                                     void* workspace, size_t ws_bytes, void* dx, float* dW_g,
+                                     float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream,
+                                     void* const* stage_events);
+
+/*
  * moe_device_status -- synchronise `stream`, then read and clear the sticky
  * device fault flag of the current device. Returns MOE_OK,
  * MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX or MOE_ERR_CUDA. Writes the

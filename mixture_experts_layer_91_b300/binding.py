@@ -34,7 +34,8 @@ EXPORTS = ["moe_status_string", "moe_version", "moe_route_workspace_size", "moe_
            "moe_permute_workspace_size",
            "moe_permute", "moe_permute_static", "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_workspace_size", "moe_forward", "moe_forward_profiled", "moe_backward_workspace_size",
-           "moe_backward", "moe_backward_profiled", "moe_device_status", "moe_debug_wait_timeout"]
+           "moe_backward", "moe_backward_profiled", "moe_forward_train", "moe_backward_from_forward",
+           "moe_device_status", "moe_debug_wait_timeout"]
 BWD_PROFILE_EVENTS = 8   # MOE_BWD_PROFILE_EVENTS
 PROFILE_EVENTS = 6   # MOE_PROFILE_EVENTS
 
@@ -100,6 +101,9 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
             "moe_backward": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, P]),
             "moe_backward_profiled": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, P,
                                             ctypes.POINTER(P)]),
+            "moe_forward_train": (I32, [C, P, P, P, P, P, P, P, P, P, SZ, P, P]),
+            "moe_backward_from_forward": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, P,
+                                                ctypes.POINTER(P)]),
             "moe_device_status": (I32, [P, ctypes.POINTER(I32)]),
             "moe_debug_wait_timeout": (I32, [ctypes.c_uint32, P]),
         }
@@ -309,15 +313,36 @@ def backward_workspace_size(cfg: MoeConfig) -> int:
     return load().moe_backward_workspace_size(ctypes.byref(cfg))
 
 
+def forward_train(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, *, workspace, y=None, stream=None):
+    """moe_forward_train: y, with the backward's state left in `workspace`
+    (a uint8 tensor of at least backward_workspace_size(cfg) bytes)."""
+    lib = load()
+    dt = act_dtype(cfg)
+    if y is None:
+        y = torch.empty(cfg.T, cfg.d, dtype=dt, device=x.device)
+    st = lib.moe_forward_train(ctypes.byref(cfg), _ptr(x, dt, "x"), _ptr(W_g, torch.float32, "W_g"),
+                               _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
+                               _ptr(bias, torch.float32, "bias", True), _ptr(W1, dt, "W1"),
+                               _ptr(W3, dt, "W3", cfg.expert_act == MOE_ACT_RELU), _ptr(W2, dt, "W2"),
+                               _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _ptr(y, dt, "y"),
+                               _stream(stream))
+    _check(st, "moe_forward_train")
+    return y
+
+
 def backward(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, *, workspace=None, out=None, events=None,
-             stream=None) -> dict:
+             from_forward=False, stream=None) -> dict:
     """moe_backward: gradients of the layer for upstream gradient dy.
     Returns a dict dx [T, d] (act dtype), dW_g [d, E], dW_noise [d, E] (noisy
     gate, else None), dW1 / dW3 [G, I, d] (dW3 None for ReLU experts) and
     dW2 [G, d, I], all fp32 but dx. `out` (a dict like the result) reuses
     output buffers; `events` (BWD_PROFILE_EVENTS torch.cuda.Event objects)
-    calls moe_backward_profiled, which records them at the stage boundaries."""
+    calls moe_backward_profiled, which records them at the stage boundaries.
+    from_forward=True calls moe_backward_from_forward on a workspace that
+    forward_train filled for the same inputs."""
     lib = load()
+    if from_forward and workspace is None:
+        raise ValueError("from_forward needs the workspace forward_train filled")
     dt = act_dtype(cfg)
     dev = x.device
     G, I, d, E = cfg.n_routed + cfg.n_shared, cfg.d_ff, cfg.d, cfg.n_routed
@@ -340,6 +365,15 @@ def backward(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, *, workspace=None,
             _ptr(out["dW_g"], f32, "dW_g"), _ptr(out["dW_noise"], f32, "dW_noise", True),
             _ptr(out["dW1"], f32, "dW1"), _ptr(out["dW3"], f32, "dW3", True), _ptr(out["dW2"], f32, "dW2"),
             _stream(stream)]
+    if from_forward:
+        arr = None
+        if events is not None:
+            for e in events:
+                if e.cuda_event == 0:
+                    e.record()
+            arr = (ctypes.c_void_p * BWD_PROFILE_EVENTS)(*[e.cuda_event for e in events])
+        _check(lib.moe_backward_from_forward(*args, arr), "moe_backward_from_forward")
+        return out
     if events is None:
         _check(lib.moe_backward(*args), "moe_backward")
         return out

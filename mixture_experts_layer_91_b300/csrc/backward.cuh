@@ -55,6 +55,20 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Rows [offsets[E], max_rows) of x_perm: left unwritten by the dispatch when an
+// expert capacity dropped assignments; cleared so that a GEMM's last k-block
+// or padding rows past the last group read finite zeros.
+template <typename TX>
+__global__ void __launch_bounds__(256)
+    zero_tail_rows_kernel(const int32_t* __restrict__ n_rows_dev, int64_t max_rows, int32_t d, TX* __restrict__ buf) {
+  const int64_t n = min(static_cast<int64_t>(__ldg(n_rows_dev)), max_rows);
+  const int64_t nvec = (max_rows - n) * d * static_cast<int64_t>(sizeof(TX)) / 16;
+  uint4* o = reinterpret_cast<uint4*>(buf + n * d);
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    o[v] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Padded row of assignment (t, j) of routed expert e = ids[t, j]: group
 // K_s + e starts at padded row 128 * mt_start[K_s + e]; dest counts from
 // a_row (= offsets[e]).

@@ -259,7 +259,9 @@ __global__ void __launch_bounds__(256)
 // the folded shared group (present when K_s > 0) holds the sum of the shared
 // experts for token t; assignment (t, j) of routed expert e = ids[t, j] sits at
 // 128 * mt_start[K_s + e] + (dest[t, j] - a_row[K_s + e]). Assignments an
-// expert's capacity refused (dest = -1) add nothing. fp32 sums in a fixed
+// expert's capacity refused (dest = -1) add nothing. With w = nullptr the
+// rows already carry their gates (g h through W2) and are summed as they are.
+// fp32 sums in a fixed
 // order (shared row, then j = 0..k-1), rounded once to bf16. One warp per
 // token; lane j < k holds assignment j's row and gate, each lane sums 8
 // columns (one 16-byte vector) per step. k <= 32. gridDim.y splits the
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(256)
     if (r >= 0) {
       const int32_t g = K_s + __ldg(ids + t * k + lane);
       my_row = 128 * __ldg(mt_start + g) + (r - __ldg(a_row + g));
-      my_g = __ldg(w + t * k + lane);
+      my_g = w != nullptr ? __ldg(w + t * k + lane) : 1.f;   // no gates: the rows carry them
     }
   }
   // the column loop is warp-uniform (the shuffles below need every lane)

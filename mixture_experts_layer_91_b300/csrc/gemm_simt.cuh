@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kSimtThreads) grouped_gemm_simt(const SimtArgs
           } else {
             const int32_t src = __ldg(p.perm_src + __ldg(p.plan.a_row + c.g) + rl);
             orow = src / p.top_k;
-            gate = __ldg(p.topk_w + src);
+            gate = p.topk_w != nullptr ? __ldg(p.topk_w + src) : 1.f;   // null: rows carry their gates
           }
         } else {
           orow = static_cast<int64_t>(__ldg(p.plan.o_row + c.g)) + rl;

@@ -495,7 +495,8 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
                           const void* W2, void* H, int mode, void* out, const int32_t* perm_src,
                           const float* topk_w, cudaStream_t st,
                           const std::function<moe_status(int)>* mark = nullptr,
-                          float* zero = nullptr, int64_t zero_n4 = 0) {
+                          float* zero = nullptr, int64_t zero_n4 = 0, bool down_only = false) {
+  // down_only: H is given (the training forward's g h rows); only the down projection runs
   const int G = n_groups(c);
   const int64_t P = padded_rows(c);
   const int I = c->d_ff, d = c->d;
@@ -536,8 +537,10 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.n_out = I;
     a.zero_out = reinterpret_cast<float4*>(zero);
     a.zero_n4 = zero != nullptr ? zero_n4 : 0;
-    grouped_gemm_tc<kEpiSwiGLU><<<grid, kTcThreads, tc_smem_bytes(kEpiSwiGLU), st>>>(gu, a);
-    MOE_TRY(last_launch());
+    if (!down_only) {
+      grouped_gemm_tc<kEpiSwiGLU><<<grid, kTcThreads, tc_smem_bytes(kEpiSwiGLU), st>>>(gu, a);
+      MOE_TRY(last_launch());
+    }
     if (mark) MOE_TRY((*mark)(3));
 
     a.K = I;
@@ -576,8 +579,10 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
   a.b1 = static_cast<const float*>(W3);
   a.relu = c->expert_act == MOE_ACT_RELU ? 1 : 0;
   a.h_out = static_cast<float*>(H);
-  grouped_gemm_simt<kEpiSwiGLU><<<grid, kSimtThreads, 0, st>>>(a);
-  MOE_TRY(last_launch());
+  if (!down_only) {
+    grouped_gemm_simt<kEpiSwiGLU><<<grid, kSimtThreads, 0, st>>>(a);
+    MOE_TRY(last_launch());
+  }
   if (mark) MOE_TRY((*mark)(3));
   a.K = I;
   a.n_out = d;
@@ -1112,11 +1117,14 @@ size_t moe_backward_workspace_size(const moe_config* cfg) {
   return backward_layout(cfg).total;
 }
 
-moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
-                                 const float* eps, const float* bias, const void* W1, const void* W3,
-                                 const void* W2, const void* dy, void* workspace, size_t ws_bytes, void* dx,
-                                 float* dW_g, float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream,
-                                 void* const* stage_events) {
+// The backward. from_state: the workspace holds what moe_forward_train left
+// (routing, logits, dispatch, plan, x_perm, a, b, g h) for these inputs, so
+// the routing, the dispatch and the gate-up recompute are skipped.
+static moe_status backward_impl(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                                const float* eps, const float* bias, const void* W1, const void* W3,
+                                const void* W2, const void* dy, void* workspace, size_t ws_bytes, void* dx,
+                                float* dW_g, float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream,
+                                void* const* stage_events, bool from_state) {
   MOE_TRY(check_config(cfg));
   const bool noisy = cfg->gate == MOE_GATE_NOISY;
   const bool swiglu = cfg->expert_act == MOE_ACT_SWIGLU;
@@ -1164,8 +1172,9 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
   float* logits = at<float>(workspace, L.logits);
   float* noise = noisy ? at<float>(workspace, L.noise) : nullptr;
   // 1. the forward's routing, recomputed (logits and noise logits kept)
-  MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w, logits,
-                       nullptr, ds->sm_count, at<void>(workspace, L.planes), st, nullptr, noise));
+  if (!from_state)
+    MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w, logits,
+                         nullptr, ds->sm_count, at<void>(workspace, L.planes), st, nullptr, noise));
   // 2. dispatch and group plan, recomputed; dy gathered into the same row order
   PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
              at<int32_t>(workspace, L.a_row), at<int32_t>(workspace, L.o_row)};
@@ -1174,8 +1183,9 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
   int32_t* offsets = at<int32_t>(workspace, L.offsets);
   void* x_perm = at<void>(workspace, L.x_perm);
   void* dy_perm = at<void>(workspace, L.dy_perm);
-  MOE_TRY(launch_permute(cfg, ds, x, ids, at<int32_t>(workspace, L.blk), at<int32_t>(workspace, L.rank),
-                         at<int32_t>(workspace, L.counts), offsets, dest, perm_src, x_perm, &po, st));
+  if (!from_state)
+    MOE_TRY(launch_permute(cfg, ds, x, ids, at<int32_t>(workspace, L.blk), at<int32_t>(workspace, L.rank),
+                           at<int32_t>(workspace, L.counts), offsets, dest, perm_src, x_perm, &po, st));
   {
     const int64_t n = n_assign(cfg);
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 7) / 8, 16ll * ds->sm_count));
@@ -1210,8 +1220,8 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
   q.dW3 = dW3;
   q.dW2 = dW2;
   MOE_TRY(mark(1));
-  // 3. a, b, g*h; then dh = dy W2 with da, db and the gates' partials
-  MOE_TRY(launch_bwd_stage(cfg, ds, 0, gp, q, st));
+  // 3. a, b, g*h (kept by moe_forward_train); then dh = dy W2 with da, db and the gates' partials
+  if (!from_state) MOE_TRY(launch_bwd_stage(cfg, ds, 0, gp, q, st));
   MOE_TRY(mark(2));
   MOE_TRY(launch_bwd_stage(cfg, ds, 1, gp, q, st));
   MOE_TRY(mark(3));
@@ -1280,12 +1290,109 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
   return mark(7);
 }
 
+moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                                 const float* eps, const float* bias, const void* W1, const void* W3,
+                                 const void* W2, const void* dy, void* workspace, size_t ws_bytes, void* dx,
+                                 float* dW_g, float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream,
+                                 void* const* stage_events) {
+  return backward_impl(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, workspace, ws_bytes, dx, dW_g, dW_noise,
+                       dW1, dW3, dW2, stream, stage_events, false);
+}
+
 moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
                         const float* eps, const float* bias, const void* W1, const void* W3, const void* W2,
                         const void* dy, void* workspace, size_t ws_bytes, void* dx, float* dW_g,
                         float* dW_noise, float* dW1, float* dW3, float* dW2, void* stream) {
-  return moe_backward_profiled(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, workspace, ws_bytes, dx, dW_g,
-                               dW_noise, dW1, dW3, dW2, stream, nullptr);
+  return backward_impl(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, workspace, ws_bytes, dx, dW_g, dW_noise,
+                       dW1, dW3, dW2, stream, nullptr, false);
+}
+
+moe_status moe_backward_from_forward(const moe_config* cfg, const void* x, const float* W_g,
+                                     const float* W_noise, const float* eps, const float* bias, const void* W1,
+                                     const void* W3, const void* W2, const void* dy, void* workspace,
+                                     size_t ws_bytes, void* dx, float* dW_g, float* dW_noise, float* dW1,
+                                     float* dW3, float* dW2, void* stream, void* const* stage_events) {
+  return backward_impl(cfg, x, W_g, W_noise, eps, bias, W1, W3, W2, dy, workspace, ws_bytes, dx, dW_g, dW_noise,
+                       dW1, dW3, dW2, stream, stage_events, true);
+}
+
+moe_status moe_forward_train(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                             const float* eps, const float* bias, const void* W1, const void* W3, const void* W2,
+                             void* workspace, size_t ws_bytes, void* y, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const bool noisy = cfg->gate == MOE_GATE_NOISY;
+  const bool swiglu = cfg->expert_act == MOE_ACT_SWIGLU;
+  if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (x == nullptr || W_g == nullptr || W1 == nullptr || (swiglu && W3 == nullptr) || W2 == nullptr ||
+      workspace == nullptr || y == nullptr || (noisy && (W_noise == nullptr || eps == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(workspace) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const BwdWs L = backward_layout(cfg);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceState* ds;
+  MOE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf = cfg->act_dtype == MOE_DT_BF16;
+  const int E = cfg->n_routed;
+  int32_t* ids = at<int32_t>(workspace, L.ids);
+  float* w = at<float>(workspace, L.w);
+  // 1. routing, keeping the logits (and noise logits) for the backward; the
+  // fp32 router also clears y, the fp32 scatter-add's target
+  MOE_TRY(launch_route(cfg, x, W_g, noisy ? W_noise : nullptr, noisy ? eps : nullptr, bias, ids, w,
+                       at<float>(workspace, L.logits), bf ? nullptr : static_cast<float*>(y), ds->sm_count,
+                       at<void>(workspace, L.planes), st, nullptr, noisy ? at<float>(workspace, L.noise) : nullptr));
+  // 2. dispatch and plan; the rows past the accepted count cleared
+  PlanOut po{at<int32_t>(workspace, L.mt_start), at<int32_t>(workspace, L.gsize),
+             at<int32_t>(workspace, L.a_row), at<int32_t>(workspace, L.o_row)};
+  int32_t* perm_src = at<int32_t>(workspace, L.perm_src);
+  int32_t* dest = at<int32_t>(workspace, L.dest);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  void* x_perm = at<void>(workspace, L.x_perm);
+  MOE_TRY(launch_permute(cfg, ds, x, ids, at<int32_t>(workspace, L.blk), at<int32_t>(workspace, L.rank),
+                         at<int32_t>(workspace, L.counts), offsets, dest, perm_src, x_perm, &po, st));
+  {
+    const int64_t n = n_assign(cfg);
+    const unsigned grid = static_cast<unsigned>(4 * ds->sm_count);
+    if (bf)
+      zero_tail_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(offsets + E, n, cfg->d,
+                                                                 static_cast<__nv_bfloat16*>(x_perm));
+    else
+      zero_tail_rows_kernel<float><<<grid, 256, 0, st>>>(offsets + E, n, cfg->d, static_cast<float*>(x_perm));
+    MOE_TRY(last_launch());
+  }
+  // 3. a, b and g h (the backward's saved state)
+  GroupPlan gp{po.mt_start, po.gsize, po.a_row, po.o_row};
+  BwdPtrs q{};
+  q.x = x;
+  q.x_perm = x_perm;
+  q.W1 = W1;
+  q.W3 = W3;
+  q.W2 = W2;
+  q.perm_src = perm_src;
+  q.topk_w = w;
+  q.a_pre = at<void>(workspace, L.a_pre);
+  q.b_pre = at<void>(workspace, L.b_pre);
+  q.hg = at<void>(workspace, L.hg);
+  MOE_TRY(launch_bwd_stage(cfg, ds, 0, gp, q, st));
+  // 4. y = sum of the rows (g h) W2^T: the gates already ride on g h, so the
+  // down projection and the combine take no gates (the same sum as moe_forward)
+  if (bf) {
+    void* rows = at<void>(workspace, L.rows);
+    MOE_TRY(launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, q.hg, kEpiStoreBf16, rows, perm_src, nullptr, st,
+                           nullptr, nullptr, 0, true));
+    const int64_t tblocks = (cfg->T + 7) / 8;
+    const int64_t ysplit = std::max<int64_t>(1, std::min<int64_t>((cfg->d + 255) / 256, 4ll * ds->sm_count / tblocks));
+    const dim3 grid(static_cast<unsigned>(tblocks), static_cast<unsigned>(ysplit));
+    combine_rows_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(rows), dest, ids, nullptr,
+                                                   po.mt_start, po.a_row, cfg->T, cfg->d, cfg->top_k,
+                                                   cfg->n_shared, static_cast<__nv_bfloat16*>(y));
+    return last_launch();
+  }
+  return launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, q.hg, kEpiScatterAdd, y, perm_src, nullptr, st,
+                        nullptr, nullptr, 0, true);
 }
 
 moe_status moe_device_status(void* stream, int32_t* raw) {

@@ -136,3 +136,43 @@ def test_backward_no_tokens_gives_zero_weight_gradients(cuda_lib):
     out = binding.backward(cfg, x, g["W_g"], None, None, None, g["W1"], g["W3"], g["W2"], x)
     for n in ("dW_g", "dW1", "dW3", "dW2"):
         assert torch.count_nonzero(out[n]).item() == 0, n
+
+
+TRAIN = [workloads.TINY_FP32, TINY_NOISY, RAGGED, workloads.DSMOE_16B.with_tokens(333), GSHARD_RELU_SMALL,
+         DSMOE_16B_CAP]
+
+
+@pytest.mark.parametrize("w", TRAIN, ids=lambda w: w.name)
+def test_forward_train_then_backward_from_forward(w, cuda_lib):
+    """moe_forward_train's y matches the oracle forward and moe_forward;
+    moe_backward_from_forward on its state gives moe_backward's gradients
+    (bitwise for bf16 layers: the same kernels on the same inputs)."""
+    inp = inputs.make_inputs(w)
+    dy, ok = upstream(w, inp)
+    cfg = binding.config(w)
+    g = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    ws = torch.empty(binding.backward_workspace_size(cfg), dtype=torch.uint8, device=DEV)
+    ws.fill_(0xFF)
+    fw = (cfg, g["x"], g["W_g"], g["W_noise"], g["eps"], g["bias"], g["W1"], g["W3"], g["W2"])
+    y = binding.forward_train(*fw, workspace=ws)
+    assert binding.device_status()[0] == 0
+    # y against the oracle on the tokens whose routing is unambiguous
+    r = O.route(inp["x"], inp["W_g"], w.top_k, renormalize=w.renormalize, noisy=w.noisy,
+                W_noise=inp["W_noise"], eps=inp["eps"], bias=inp["bias"])
+    toks = np.nonzero(ok)[0]
+    keep = O.capacity_keep(r["ids"], w.n_routed, w.capacity) if w.capacity else None
+    ref_y = O.moe_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], w.n_shared, r["ids"], r["gates"],
+                          tokens=toks, act=w.act, keep=keep)
+    check_close(y.float().cpu().numpy()[toks], ref_y, w.fp32, f"{w.name} forward_train y")
+    y_ref = binding.forward(*fw)
+    check_close(y.float().cpu().numpy()[toks], y_ref.float().cpu().numpy()[toks], w.fp32, "vs moe_forward")
+    ref = binding.backward(*fw, dy.to(DEV))
+    got = binding.backward(*fw, dy.to(DEV), workspace=ws, from_forward=True)
+    assert binding.device_status()[0] == 0
+    for n in ("dx", "dW_g", "dW_noise", "dW1", "dW3", "dW2"):
+        if got[n] is None:
+            continue
+        if w.fp32:   # the fp32 router-weight gradient sums chunks with atomics
+            torch.testing.assert_close(got[n], ref[n], rtol=1e-5, atol=1e-7)
+        else:
+            assert torch.equal(got[n], ref[n]), n
