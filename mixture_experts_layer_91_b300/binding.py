@@ -165,10 +165,11 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def route(cfg, x, W_g, W_noise=None, eps=None, bias=None, *, want_logits=False, want_stats=False,
-          stream=None):
+          workspace=None, stream=None):
     """moe_route. Returns (ids, gates), plus logits [T, E] with want_logits,
     plus a dict of router statistics (lse [T], prob_sum [E], gate_sum [E])
-    with want_stats."""
+    with want_stats. `workspace`: a uint8 device tensor of at least
+    route_workspace_size(cfg) bytes (allocated here when None)."""
     lib = load()
     T, k, E = cfg.T, cfg.top_k, cfg.n_routed
     dev = x.device
@@ -182,7 +183,7 @@ def route(cfg, x, W_g, W_noise=None, eps=None, bias=None, *, want_logits=False, 
                  "gate_sum": torch.empty(E, dtype=torch.float32, device=dev)}
         stats_c = RouterStats(stats["lse"].data_ptr(), stats["prob_sum"].data_ptr(),
                               stats["gate_sum"].data_ptr())
-    ws = _workspace(route_workspace_size(cfg), dev)
+    ws = _workspace(route_workspace_size(cfg), dev) if workspace is None else workspace
     st = lib.moe_route(ctypes.byref(cfg), _ptr(x, act_dtype(cfg), "x"), _ptr(W_g, torch.float32, "W_g"),
                        _ptr(W_noise, torch.float32, "W_noise", True), _ptr(eps, torch.float32, "eps", True),
                        _ptr(bias, torch.float32, "bias", True), ids.data_ptr(), w.data_ptr(),

@@ -30,6 +30,8 @@ constexpr int kCountPerWarp = kCountBlock / (kCountThreads / 32);
 __global__ void __launch_bounds__(kCountThreads)
     count_kernel(const int32_t* __restrict__ ids, int64_t n, int32_t E,
                  int32_t* __restrict__ blk_hist, int32_t* __restrict__ local_rank) {
+  pdl_wait();   // launched as a programmatic dependent: inputs ready from here on
+  pdl_launch_dependents();
   extern __shared__ int32_t wh[];   // [8][E] per-warp counts
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 8 * E; i += kCountThreads) wh[i] = 0;
@@ -133,6 +135,8 @@ __global__ void __launch_bounds__(kScanThreads)
     scan_kernel(int32_t* __restrict__ blk_hist, int32_t nblk, int32_t E, int32_t capacity,
                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t K_s, int64_t T,
                 PlanOut plan, int32_t with_plan) {
+  pdl_wait();   // launched as a programmatic dependent: inputs ready from here on
+  pdl_launch_dependents();
   __shared__ int32_t tot[kMaxGroups + 1];
   __shared__ int32_t part[kScanThreads];
   // split the block range of each expert over `parts` threads
@@ -196,6 +200,8 @@ __global__ void __launch_bounds__(256)
                    const int32_t* __restrict__ offsets, int32_t capacity,
                    const TX* __restrict__ x, int32_t d, int32_t* __restrict__ dest,
                    int32_t* __restrict__ perm_src, TX* __restrict__ x_perm) {
+  pdl_wait();   // launched as a programmatic dependent: inputs ready from here on
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t nvec = static_cast<int64_t>(d) * sizeof(TX) / 16;
@@ -272,6 +278,8 @@ __global__ void __launch_bounds__(256)
                              const int32_t* __restrict__ ids, const float* __restrict__ w,
                              const int32_t* __restrict__ mt_start, const int32_t* __restrict__ a_row,
                              int64_t T, int32_t d, int32_t k, int32_t K_s, __nv_bfloat16* __restrict__ y) {
+  pdl_wait();   // launched as a programmatic dependent: inputs ready from here on
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;   // warp-uniform

@@ -201,6 +201,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent: the prologue above overlapped the
+  // previous kernel; the plan, the operands and the outputs are touched only
+  // from here on.
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int32_t folded = p.fold_mt > 0 ? (p.n_shared - 1) * p.fold_mt : 0;
   const int32_t total = (__ldg(p.plan.mt_start + p.G) - folded) * p.n_tiles;

@@ -26,7 +26,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kVersion = (2 << 16) | 2;
+constexpr int kVersion = (2 << 16) | 3;
 constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------------------------------
@@ -83,6 +83,37 @@ int router_tc_np(const moe_config* c) {
 size_t router_planes_bytes(const moe_config* c) {
   return static_cast<size_t>(3) * router_tc_np(c) * c->d * 2;
 }
+
+// The CUDA-core router's k-groups (RouterArgs::kgroups): at most 16, and only
+// for T <= 512 (16 token blocks), where one cluster per token block leaves
+// most SMs idle.
+constexpr int kRouterMaxGroups = 16;
+constexpr int64_t kRouterGroupMaxTokens = 512;
+constexpr int kRouterMaxCluster = 8;
+
+int router_epad(const moe_config* c) {
+  const int cols = router_cols(c);
+  return cols <= 32 ? 32 : (cols <= 64 ? 64 : (cols <= 128 ? 128 : 256));
+}
+
+// Bytes of the k-groups' partial rows ([block][group][32][EPAD] fp32) and
+// arrival counters ([block][cluster rank] int32); 0 where no k-groups run.
+size_t router_group_part_bytes(const moe_config* c) {
+  if (router_tc_np(c) > 0 || c->T == 0 || c->T > kRouterGroupMaxTokens) return 0;
+  const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
+  return (static_cast<size_t>(nblk) * kRouterMaxGroups * kRouterBT * router_epad(c) * 4 + 255) &
+         ~static_cast<size_t>(255);
+}
+size_t router_group_bytes(const moe_config* c) {
+  const size_t part = router_group_part_bytes(c);
+  if (part == 0) return 0;
+  const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
+  return part + static_cast<size_t>(nblk) * kRouterMaxCluster * 4;
+}
+
+// Scratch of launch_route: the planes (tensor-core router) or the k-groups'
+// rows and counters (CUDA-core router, few tokens); at most one is non-zero.
+size_t router_scratch_bytes(const moe_config* c) { return router_planes_bytes(c) + router_group_bytes(c); }
 
 // ---------------------------------------------------------------------------
 // workspace layouts (every region 256-byte aligned)
@@ -161,7 +192,7 @@ FwdWs forward_layout(const moe_config* c) {
   const bool bf = c->act_dtype == MOE_DT_BF16;
   w.y_acc = bf && !rows_combine(c) ? k.take(sizeof(float) * c->T * c->d) : 0;
   w.rows = rows_combine(c) ? k.take(sizeof(__nv_bfloat16) * padded_rows(c) * c->d) : 0;
-  w.planes = k.take(router_planes_bytes(c));
+  w.planes = k.take(router_scratch_bytes(c));
   w.total = k.off;
   return w;
 }
@@ -222,7 +253,7 @@ BwdWs backward_layout(const moe_config* c) {
   w.D = bwd_tc(c) ? 0 : k.take(sizeof(float) * c->T * cols);
   w.rows = k.take(ab * P * c->d);
   w.dxr = k.take(sizeof(float) * c->T * c->d);
-  w.planes = k.take(router_planes_bytes(c));
+  w.planes = k.take(router_scratch_bytes(c));
   const bool tc = bwd_tc(c);
   const int nc = rg_chunks(c);
   w.gplanes = tc ? k.take(sizeof(__nv_bfloat16) * 3 * rg_rows(c) * rg_ep(c)) : 0;
@@ -361,12 +392,37 @@ moe_status last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : M
     if (_s != MOE_OK) return _s;        \
   } while (0)
 
+// Launch `kernel` as a programmatic dependent of the stream's previous kernel
+// (programmatic stream serialization): its CTAs may start while that kernel
+// drains, and the kernel itself calls griddepcontrol.wait before it touches
+// memory that earlier work writes or reads. Every kernel launched this way
+// does so.
+template <typename... Params, typename... Args>
+moe_status launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t lc{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return last_launch();
+}
+
 // ---------------------------------------------------------------------------
 // stages
 // ---------------------------------------------------------------------------
 moe_status launch_route(const moe_config* c, const void* x, const float* W_g, const float* W_noise,
                         const float* eps, const float* bias, int32_t* ids, float* w, float* logits,
-                        float* zero_rows, int sm_count, void* planes, cudaStream_t st,
+                        float* zero_rows, int sm_count, void* scratch, cudaStream_t st,
                         const moe_router_stats* stats = nullptr, float* noise_logits = nullptr) {
   RouterArgs a;
   a.x = x;
@@ -390,6 +446,9 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   a.lse = stats ? stats->lse : nullptr;
   a.prob_sum = stats ? stats->prob_sum : nullptr;
   a.gate_sum = stats ? stats->gate_sum : nullptr;
+  a.part = nullptr;
+  a.part_count = nullptr;
+  a.kgroups = 1;
   if (c->T > 0) {   // the per-expert sums are accumulated with atomics
     if (a.prob_sum && cudaMemsetAsync(a.prob_sum, 0, sizeof(float) * c->n_routed, st) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -401,7 +460,7 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   if (np > 0) {
     if (c->T == 0) return MOE_OK;
     // split [W_g | W_noise] into three bf16 planes, then the tensor-core router
-    auto* pl = static_cast<__nv_bfloat16*>(planes);
+    auto* pl = static_cast<__nv_bfloat16*>(scratch);
     router_split_kernel<<<dim3(static_cast<unsigned>((c->d + 31) / 32), static_cast<unsigned>(np / 32)), 256, 0,
                           st>>>(W_g, W_noise, c->d, c->n_routed, cols, np, pl);
     MOE_TRY(last_launch());
@@ -410,13 +469,32 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
                      CU_TENSOR_MAP_SWIZZLE_128B));
     MOE_TRY(make_map(&wm, pl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->d, 3ull * np, 64, np,
                      CU_TENSOR_MAP_SWIZZLE_128B));
-    const unsigned grid = static_cast<unsigned>((c->T + 127) / 128);
-    if (np == 32)
-      router_tc_kernel<32><<<grid, kRtcThreads, RtcShape<32>::smem_bytes, st>>>(xm, wm, a);
-    else if (np == 64)
-      router_tc_kernel<64><<<grid, kRtcThreads, RtcShape<64>::smem_bytes, st>>>(xm, wm, a);
-    else
-      router_tc_kernel<128><<<grid, kRtcThreads, RtcShape<128>::smem_bytes, st>>>(xm, wm, a);
+    // launched as the split kernel's programmatic dependent: its prologue and
+    // first x loads overlap the split, and its producer waits for the planes
+    cudaLaunchConfig_t lc{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = dim3(static_cast<unsigned>((c->T + 127) / 128), 1, 1);
+    lc.blockDim = dim3(kRtcThreads, 1, 1);
+    lc.stream = st;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t e;
+    if (np == 32) {
+      lc.dynamicSmemBytes = RtcShape<32>::smem_bytes;
+      e = cudaLaunchKernelEx(&lc, router_tc_kernel<32>, xm, wm, a);
+    } else if (np == 64) {
+      lc.dynamicSmemBytes = RtcShape<64>::smem_bytes;
+      e = cudaLaunchKernelEx(&lc, router_tc_kernel<64>, xm, wm, a);
+    } else {
+      lc.dynamicSmemBytes = RtcShape<128>::smem_bytes;
+      e = cudaLaunchKernelEx(&lc, router_tc_kernel<128>, xm, wm, a);
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
     return last_launch();
   }
   const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
@@ -425,10 +503,24 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   // k-chunks, until there are about two CTAs per SM or two chunks per CTA.
   const int nchunk = (c->d + 63) / 64;   // the smallest k-chunk of any router shape
   int cs = 1;
-  while (cs < 8 && nblk * cs < 2ll * sm_count && nchunk >= 4 * cs) cs *= 2;
+  while (cs < kRouterMaxCluster && nblk * cs < 2ll * sm_count && nchunk >= 4 * cs) cs *= 2;
+  // Still far fewer CTAs than SMs (T <= 512): k-groups of clusters, until
+  // about one CTA per SM or one chunk per CTA.
+  int kg = 1;
+  if (router_group_bytes(c) > 0)
+    while (2 * kg <= kRouterMaxGroups && nblk * cs * 2 * kg <= sm_count && nchunk >= cs * 2 * kg) kg *= 2;
+  if (kg > 1) {
+    a.kgroups = kg;
+    a.part = static_cast<float*>(scratch);
+    a.part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + router_group_part_bytes(c));
+    if (cudaMemsetAsync(a.part_count, 0, sizeof(int32_t) * nblk * cs, st) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  }
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[1];
-  lc.gridDim = dim3(static_cast<unsigned>(nblk * cs), 1, 1);
+  lc.gridDim = dim3(static_cast<unsigned>(nblk * kg * cs), 1, 1);
   lc.blockDim = dim3(kRouterThreads, 1, 1);
   lc.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -463,26 +555,24 @@ moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void
   const int64_t nblk = n_count_blocks(c);
   const int E = c->n_routed;
   if (nblk > 0) {
-    count_kernel<<<static_cast<unsigned>(nblk), kCountThreads, 8 * E * sizeof(int32_t), st>>>(
-        ids, n, E, blk, rank);
-    MOE_TRY(last_launch());
+    MOE_TRY(launch_dependent(count_kernel, dim3(static_cast<unsigned>(nblk)), dim3(kCountThreads),
+                             8 * E * sizeof(int32_t), st, ids, n, E, blk, rank));
   }
   PlanOut none{};
-  scan_kernel<<<1, kScanThreads, 0, st>>>(blk, static_cast<int32_t>(nblk), E, c->capacity, counts,
-                                          offsets, c->n_shared, c->T, plan ? *plan : none, plan ? 1 : 0);
-  MOE_TRY(last_launch());
+  MOE_TRY(launch_dependent(scan_kernel, dim3(1), dim3(kScanThreads), 0, st, blk, static_cast<int32_t>(nblk), E,
+                           c->capacity, counts, offsets, c->n_shared, c->T, plan ? *plan : none,
+                           static_cast<int32_t>(plan ? 1 : 0)));
   if (n > 0) {
     const int64_t want = (n + 7) / 8;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, 16ll * ds->sm_count));
     if (c->act_dtype == MOE_DT_BF16)
-      scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-          ids, n, c->top_k, E, blk, rank, offsets, c->capacity, static_cast<const __nv_bfloat16*>(x),
-          c->d, dest, perm_src, static_cast<__nv_bfloat16*>(x_perm));
+      MOE_TRY(launch_dependent(scatter_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, ids, n, c->top_k, E,
+                               blk, rank, offsets, c->capacity, static_cast<const __nv_bfloat16*>(x), c->d,
+                               dest, perm_src, static_cast<__nv_bfloat16*>(x_perm)));
     else
-      scatter_kernel<float><<<grid, 256, 0, st>>>(ids, n, c->top_k, E, blk, rank, offsets, c->capacity,
-                                                        static_cast<const float*>(x), c->d, dest,
-                                                        perm_src, static_cast<float*>(x_perm));
-    MOE_TRY(last_launch());
+      MOE_TRY(launch_dependent(scatter_kernel<float>, dim3(grid), dim3(256), 0, st, ids, n, c->top_k, E, blk,
+                               rank, offsets, c->capacity, static_cast<const float*>(x), c->d, dest, perm_src,
+                               static_cast<float*>(x_perm)));
   }
   return MOE_OK;
 }
@@ -537,10 +627,9 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.n_out = I;
     a.zero_out = reinterpret_cast<float4*>(zero);
     a.zero_n4 = zero != nullptr ? zero_n4 : 0;
-    if (!down_only) {
-      grouped_gemm_tc<kEpiSwiGLU><<<grid, kTcThreads, tc_smem_bytes(kEpiSwiGLU), st>>>(gu, a);
-      MOE_TRY(last_launch());
-    }
+    if (!down_only)
+      MOE_TRY(launch_dependent(grouped_gemm_tc<kEpiSwiGLU>, dim3(grid), dim3(kTcThreads),
+                               tc_smem_bytes(kEpiSwiGLU), st, gu, a));
     if (mark) MOE_TRY((*mark)(3));
 
     a.K = I;
@@ -554,12 +643,14 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     const bool fold = (mode == kEpiScatterAdd || mode == kEpiStoreBf16) && c->n_shared > 0;
     a.fold_mt = fold ? static_cast<int32_t>((c->T + kTcBM - 1) / kTcBM) : 0;
     if (mode == kEpiStoreBf16)
-      grouped_gemm_tc<kEpiStoreBf16><<<grid, kTcThreads, tc_smem_bytes(kEpiStoreBf16), st>>>(dn, a);
+      MOE_TRY(launch_dependent(grouped_gemm_tc<kEpiStoreBf16>, dim3(grid), dim3(kTcThreads),
+                               tc_smem_bytes(kEpiStoreBf16), st, dn, a));
     else if (mode == kEpiScatterAdd)
-      grouped_gemm_tc<kEpiScatterAdd><<<grid, kTcThreads, tc_smem_bytes(kEpiScatterAdd), st>>>(dn, a);
+      MOE_TRY(launch_dependent(grouped_gemm_tc<kEpiScatterAdd>, dim3(grid), dim3(kTcThreads),
+                               tc_smem_bytes(kEpiScatterAdd), st, dn, a));
     else
-      grouped_gemm_tc<kEpiStoreRows><<<grid, kTcThreads, tc_smem_bytes(kEpiStoreRows), st>>>(dn, a);
-    MOE_TRY(last_launch());
+      MOE_TRY(launch_dependent(grouped_gemm_tc<kEpiStoreRows>, dim3(grid), dim3(kTcThreads),
+                               tc_smem_bytes(kEpiStoreRows), st, dn, a));
     return mark ? (*mark)(4) : MOE_OK;
   }
   SimtArgs a{};
@@ -893,7 +984,7 @@ int moe_version(void) { return kVersion; }
 
 size_t moe_route_workspace_size(const moe_config* cfg) {
   if (check_config(cfg) != MOE_OK) return 0;
-  return router_planes_bytes(cfg);
+  return router_scratch_bytes(cfg);
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
@@ -907,7 +998,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_g, con
   if (noisy && cfg->T > 0 && (W_noise == nullptr || eps == nullptr)) return MOE_ERR_INVALID_ARG;
   if (noisy && bias != nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
-  const size_t need = router_planes_bytes(cfg);
+  const size_t need = router_scratch_bytes(cfg);
   if (ws_bytes < need || (need > 0 && workspace == nullptr)) return MOE_ERR_WORKSPACE;
   DeviceState* ds;
   MOE_TRY(device_state(&ds));
@@ -1089,11 +1180,10 @@ moe_status moe_forward_profiled(const moe_config* cfg, const void* x, const floa
     const int64_t slices = (cfg->d + 255) / 256;
     const int64_t ysplit = std::max<int64_t>(1, std::min<int64_t>(slices, 4ll * ds->sm_count / tblocks));
     const dim3 grid(static_cast<unsigned>(tblocks), static_cast<unsigned>(ysplit));
-    combine_rows_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(rows),
-                                                   at<int32_t>(workspace, L.dest), ids, w, po.mt_start,
-                                                   po.a_row, cfg->T, cfg->d, cfg->top_k, cfg->n_shared,
-                                                   static_cast<__nv_bfloat16*>(y));
-    MOE_TRY(last_launch());
+    MOE_TRY(launch_dependent(combine_rows_bf16_kernel, grid, dim3(256), 0, st,
+                             static_cast<const __nv_bfloat16*>(rows), at<int32_t>(workspace, L.dest), ids, w,
+                             po.mt_start, po.a_row, cfg->T, cfg->d, cfg->top_k, cfg->n_shared,
+                             static_cast<__nv_bfloat16*>(y)));
   } else if (bf) {
     const int64_t n8 = cfg->T * cfg->d / 8;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n8 + 255) / 256, 8ll * ds->sm_count));
@@ -1386,10 +1476,10 @@ moe_status moe_forward_train(const moe_config* cfg, const void* x, const float* 
     const int64_t tblocks = (cfg->T + 7) / 8;
     const int64_t ysplit = std::max<int64_t>(1, std::min<int64_t>((cfg->d + 255) / 256, 4ll * ds->sm_count / tblocks));
     const dim3 grid(static_cast<unsigned>(tblocks), static_cast<unsigned>(ysplit));
-    combine_rows_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(rows), dest, ids, nullptr,
-                                                   po.mt_start, po.a_row, cfg->T, cfg->d, cfg->top_k,
-                                                   cfg->n_shared, static_cast<__nv_bfloat16*>(y));
-    return last_launch();
+    return launch_dependent(combine_rows_bf16_kernel, grid, dim3(256), 0, st,
+                            static_cast<const __nv_bfloat16*>(rows), dest, ids, static_cast<const float*>(nullptr),
+                            po.mt_start, po.a_row, cfg->T, cfg->d, cfg->top_k, cfg->n_shared,
+                            static_cast<__nv_bfloat16*>(y));
   }
   return launch_experts(cfg, ds, x, x_perm, gp, W1, W3, W2, q.hg, kEpiScatterAdd, y, perm_src, nullptr, st,
                         nullptr, nullptr, 0, true);

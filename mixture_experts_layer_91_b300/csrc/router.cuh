@@ -20,8 +20,11 @@
 // memory in a fixed order. When T is small a thread-block cluster of CS CTAs
 // also splits the k-chunks; each CTA of the cluster then owns BT / CS of the
 // tokens and adds their partial rows from every CTA's tile through
-// distributed shared memory (ranks in order). Per token, one warp computes the
-// softmax and a k-round warp arg-max (ties to the lower index).
+// distributed shared memory (ranks in order). With very few tokens, k-groups
+// of such clusters split the chunks further: each writes its rows to global
+// scratch, and the last group to arrive for a token share sums them in group
+// order. Per token, one warp computes the softmax and a k-round warp arg-max
+// (ties to the lower index).
 #pragma once
 
 #include "common.cuh"
@@ -47,6 +50,15 @@ struct RouterArgs {
   float* lse;
   float* prob_sum;
   float* gate_sum;
+  // k-groups (CUDA-core router, few tokens): kgroups clusters share one token
+  // block, each over every kgroups-th run of k-chunks; their partial logits
+  // rows meet in `part` ([block][group][BT][EPAD] fp32), and per token share
+  // (block, cluster rank) an arrival counter `part_count` (zero at launch)
+  // picks the last group to arrive, which sums the groups in group order and
+  // finishes those tokens. kgroups = 1: no k-groups.
+  float* part;
+  int32_t* part_count;
+  int32_t kgroups;
 };
 
 constexpr int kRouterBT = 32;       // tokens per CTA
@@ -295,13 +307,17 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int tg = lane >> 3, cg = lane & 7;          // token group, column group of this lane
+  pdl_launch_dependents();   // the dispatch kernels may launch and wait for this one
   const int wr = warp / S::SPLIT;                   // warp row
   const int ks = warp % S::SPLIT;                   // k-step phase of this warp inside a chunk
   const int tok0 = wr * S::WT + tg * TM;            // first token (CTA-local) of the thread tile
 
   const uint32_t crank = cluster_rank();
   const uint32_t csize = cluster_size();
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * S::BT;
+  const int64_t cid = blockIdx.x / csize;                  // cluster
+  const int kg = static_cast<int>(cid % p.kgroups);       // its k-group
+  const int64_t tb = cid / p.kgroups;                     // its token block
+  const int64_t t0 = tb * S::BT;
   __shared__ float s_prob[EPAD], s_gate[EPAD];   // per-CTA statistic sums
   for (int c = tid; c < EPAD; c += kRouterThreads) {
     s_prob[c] = 0.f;
@@ -310,7 +326,7 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
 
   // fused clear of the fp32 accumulator rows of these tokens (forward path),
   // shared among the CTAs of the cluster
-  if (p.zero_rows != nullptr) {
+  if (p.zero_rows != nullptr && kg == 0) {
     const int64_t rows = (p.T - t0 < S::BT) ? (p.T - t0) : S::BT;
     float4* z = reinterpret_cast<float4*>(p.zero_rows + t0 * p.zero_width);
     const int64_t n4 = rows * p.zero_width / 4;
@@ -325,10 +341,13 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
+  // chunks kg * csize + crank, then every (kgroups * csize)-th
+  const int first = kg * static_cast<int>(csize) + static_cast<int>(crank);
+  const int step = p.kgroups * static_cast<int>(csize);
   if (p.w_vec4)
-    router_mainloop<TX, EPAD, 4>(p, rsm, t0, crank, csize, tid, tok0, ks, cg, acc);
+    router_mainloop<TX, EPAD, 4>(p, rsm, t0, first, step, tid, tok0, ks, cg, acc);
   else
-    router_mainloop<TX, EPAD, 1>(p, rsm, t0, crank, csize, tid, tok0, ks, cg, acc);
+    router_mainloop<TX, EPAD, 1>(p, rsm, t0, first, step, tid, tok0, ks, cg, acc);
 
   // partial tiles of the k-phases: part[ks][token][column]
   float* part = rsm;
@@ -373,6 +392,35 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
       part[tok * S::LS + col] = s;
     }
     cluster_sync_all();   // no CTA leaves while another still reads its tile
+  }
+  if (p.kgroups > 1) {
+    // This group's rows of the share go to the scratch; the last group to
+    // arrive sums every group's rows in group order (a fixed summation order
+    // whatever the arrival order) and finishes the share's tokens.
+    const int share = tok_end - tok_begin;
+    const int64_t blk0 = tb * p.kgroups * S::BT * EPAD;   // the block's first group row
+    float* mine = p.part + blk0 + static_cast<int64_t>(kg) * S::BT * EPAD;
+    for (int idx = tid; idx < share * EPAD; idx += kRouterThreads) {
+      const int tok = tok_begin + idx / EPAD, col = idx % EPAD;
+      mine[tok * EPAD + col] = part[tok * S::LS + col];
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_last;
+    int32_t* cnt = p.part_count + tb * csize + crank;
+    if (tid == 0) s_last = atomicAdd(cnt, 1) == p.kgroups - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* all = p.part + blk0;
+    for (int idx = tid; idx < share * EPAD; idx += kRouterThreads) {
+      const int tok = tok_begin + idx / EPAD, col = idx % EPAD;
+      float s = __ldcg(all + tok * EPAD + col);
+      for (int g = 1; g < p.kgroups; ++g) s += __ldcg(all + (static_cast<int64_t>(g) * S::BT + tok) * EPAD + col);
+      part[tok * S::LS + col] = s;
+    }
+    if (tid == 0) *cnt = 0;   // every group has arrived: ready for the next launch
+    __syncthreads();
   }
 
   // per-token softmax + top-k: one warp per token

@@ -20,20 +20,25 @@
 // So the logits are an fp32 dot product of the exact inputs, as the fp32
 // router asks ("Mixture of Experts" notes, section 5, ST-MoE precision).
 //
-// One CTA owns a 128-token tile; 6 warps:
+// One CTA owns a 128-token tile; 10 warps:
 //   warp 0      TMA producer: x [128 x 64] and the three W planes [NP x 64]
-//               per k-block into a multi-stage ring;
+//               per k-block into a multi-stage ring (x of the first stages is
+//               requested before the planes, which the split kernel just
+//               before writes: programmatic dependent launch);
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
 //               M=128 K=16: one N = 2 NP MMA over the stacked hi | mid planes
 //               and one N = NP MMA adding lo onto mid (lo's products are 2^-9
 //               of mid's, so sharing their accumulator costs nothing), into
 //               2-4 accumulator buffers rotated over chunks;
-//   warps 2-5   clear the tile's rows of the fp32 combine accumulator (forward
-//               path), then drain each chunk (warp w reads the TMEM lanes of
-//               quarter w % 4: one token per thread) into NP fp32 registers,
-//               and finally compute that token's softmax and top-k over its
-//               logits row in shared memory (eight interleaved arg-max chains
-//               per round, ties to the lower expert index).
+//   warps 2-9   clear the tile's rows of the fp32 combine accumulator (forward
+//               path), then drain each chunk: warp w reads the TMEM lanes of
+//               quarter w % 4 (one token per thread) and one half of the NP
+//               columns (warps 2-5 the first, 6-9 the second; at NP = 32
+//               warps 2-5 all of them) into fp32 registers. Then two adjacent lanes finish each token: softmax
+//               and top-k over its logits row in shared memory, each lane over
+//               the experts of one parity (four interleaved arg-max chains),
+//               the pair's candidates merged by one shuffle, ties to the lower
+//               expert index.
 #pragma once
 
 #include "common.cuh"
@@ -41,27 +46,30 @@
 
 namespace moe {
 
-constexpr int kRtcThreads = 192;
+constexpr int kRtcThreads = 320;
 constexpr int kRtcChunk = 2;   // k-blocks (of 64) per tensor-memory drain
 
 template <int NP>
 struct RtcShape {
   static_assert(NP == 32 || NP == 64 || NP == 128, "router tile width");
-  static constexpr int STAGES = NP <= 64 ? 4 : 3;
   static constexpr uint32_t A_BYTES = 128 * 64 * 2;   // x tile, 128 tokens x 64 k
   static constexpr uint32_t B_BYTES = NP * 64 * 2;    // one W plane, NP columns x 64 k
   static constexpr uint32_t STAGE_BYTES = A_BYTES + 3 * B_BYTES;
-  static constexpr int LS = NP + 1;                   // row stride of the per-token logits rows
-  // One accumulator buffer holds hi | (mid + lo) side by side (2 NP columns):
-  // one MMA of N = 2 NP for the stacked hi | mid planes, one of N = NP adding
-  // lo onto the mid columns (lo's products are 2^-9 of mid's, so sharing their
-  // accumulator costs nothing). Up to four buffers let the MMAs run three
-  // chunks ahead of the drains.
+  // as many stages as fit: x is the stream from HBM, and each stage in flight
+  // carries 16 KB of it
+  static constexpr int STAGES = NP == 32 ? 7 : (NP == 64 ? 5 : 3);
+  // Row stride of the per-token logits rows: with two lanes per token (one per
+  // expert parity), a warp's 16 token pairs fall on 32 distinct banks.
+  static constexpr int LS = NP + 2;
+  // One accumulator buffer holds hi | (mid + lo) side by side (2 NP columns).
+  // Up to four buffers let the MMAs run three chunks ahead of the drains.
   static constexpr uint32_t BUF_COLS = 2 * NP;
   static constexpr int NBUF = 512 / BUF_COLS < 4 ? 512 / BUF_COLS : 4;
   static constexpr uint32_t TMEM_COLS = NBUF * BUF_COLS;   // 256 or 512: a power of two
   static constexpr size_t smem_bytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256;
   static_assert(2ull * 128 * LS * 4 <= static_cast<size_t>(STAGES) * STAGE_BYTES, "epilogue rows");
+  static_assert(16 * STAGES + 16 * NBUF + 16 <= 256, "barrier area");
+  static_assert(smem_bytes <= 232448, "shared memory per CTA");
 };
 
 // The three bf16 planes of W = [W_g | W_noise] ([d, cols] fp32, row-major),
@@ -70,6 +78,7 @@ __global__ void __launch_bounds__(256)
     router_split_kernel(const float* __restrict__ W_g, const float* __restrict__ W_noise, int32_t d,
                         int32_t E, int32_t cols, int32_t NP, __nv_bfloat16* __restrict__ planes) {
   __shared__ float tile[32][33];
+  pdl_launch_dependents();   // the router's prologue and first x loads may start now
   const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
   for (int r = ty; r < 32; r += 8) {
@@ -122,6 +131,10 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                      const RouterArgs p) {
   using S = RtcShape<NP>;
+  // columns of each plane one drain thread reads: half of them, except at
+  // NP = 32, where warps 2-5 drain all 32 (whole 32-column loads) and warps
+  // 6-9 only keep step with the chunk barriers
+  constexpr int NH = NP == 32 ? 32 : NP / 2;
   extern __shared__ uint8_t rtc_smem_raw[];
   const uint32_t raw = smem_addr(rtc_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -138,6 +151,7 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 128;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::STAGES; ++s) {
@@ -146,7 +160,7 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
     }
     for (int b = 0; b < S::NBUF; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, 4);
+      mbar_init(bar_tempty + 8 * b, 8);   // one arrival per drain warp
     }
     mbar_init(bar_done, 1);
     *abort = 0;
@@ -170,7 +184,23 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      int32_t kb = 0;
+      // The first stages' x tiles go out before the wait for the kernel that
+      // writes the W planes; their W tiles follow it. Every stage's barrier
+      // expects the whole stage, so no stage completes early.
+      const int32_t head = nk < S::STAGES ? nk : S::STAGES;
+      for (int32_t kb = 0; kb < head; ++kb) {
+        const uint32_t full = bar_full + 8 * kb;
+        mbar_arrive_expect_tx(full, S::STAGE_BYTES);
+        tma_load_2d(base + kb * S::STAGE_BYTES, &xmap, full, kb * 64, static_cast<int32_t>(t0));
+      }
+      pdl_wait();
+      for (int32_t kb = 0; kb < head; ++kb) {
+        const uint32_t sa = base + kb * S::STAGE_BYTES;
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl)
+          tma_load_2d(sa + S::A_BYTES + pl * S::B_BYTES, &wmap, bar_full + 8 * kb, kb * 64, pl * NP);
+      }
+      int32_t kb = head;
       bool ok = true;
       for (; kb < nk; ++kb) {
         const uint32_t s = kb % S::STAGES;
@@ -196,7 +226,6 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(128, NP);
       bool ok = true;
       int32_t kb = 0;
       for (int32_t ch = 0; ch < nchunk && ok; ++ch) {
@@ -230,41 +259,46 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
       mbar_wait(bar_done, 0, &never, 100000000ull);
     }
     __syncwarp();
-    // the drain warps are done with tensor memory once all 160 threads meet here
-    asm volatile("bar.sync 1, 160;" ::: "memory");
+    // the drain warps are done with tensor memory once all 288 threads meet here
+    asm volatile("bar.sync 1, 288;" ::: "memory");
     tc_fence_after();
     tmem_dealloc(tmem_base, S::TMEM_COLS);
     return;
   }
 
-  // ---------------------------------------------------------------- warps 2-5
+  // ---------------------------------------------------------------- warps 2-9
   const int q = warp & 3;                       // TMEM lane quarter = token group
+  const int half = (warp - 2) >> 2;             // column half of every plane
   const int row = q * 32 + lane;                // token of this thread within the tile
+  const bool drains = NP != 32 || half == 0;
+  pdl_wait();   // the writes below wait for the kernels launched before this one
   if (p.zero_rows != nullptr) {
     const int64_t rows = (p.T - t0 < 128) ? (p.T - t0) : 128;
     float4* z = reinterpret_cast<float4*>(p.zero_rows + t0 * p.zero_width);
     const int64_t n4 = rows * p.zero_width / 4;
-    for (int64_t i = threadIdx.x - 64; i < n4; i += 128) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = threadIdx.x - 64; i < n4; i += 256) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float acc[NP];
+  float acc[NH];
 #pragma unroll
-  for (int c = 0; c < NP; ++c) acc[c] = 0.f;
+  for (int c = 0; c < NH; ++c) acc[c] = 0.f;
   bool ok = true;
-  const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + half * NH;
   for (int32_t ch = 0; ch < nchunk; ++ch) {
     const uint32_t b = ch % S::NBUF;
     ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_tfull + 8 * b, (ch / S::NBUF) & 1u, abort));
     if (!ok) break;
     tc_fence_after();
+    if (drains) {
 #pragma unroll
-    for (int cc = 0; cc < NP / 32; ++cc) {
-      const uint32_t col = tl + b * S::BUF_COLS + cc * 32;
-      uint32_t hi[32], ml[32];
-      tmem_ld_32x32b_x32(col, hi);
-      tmem_ld_32x32b_x32(col + NP, ml);
-      tmem_ld_wait();
+      for (int cc = 0; cc < NH / 32; ++cc) {
+        const uint32_t col = tl + b * S::BUF_COLS + cc * 32;
+        uint32_t hi[32], ml[32];
+        tmem_ld_32x32b_x32(col, hi);
+        tmem_ld_32x32b_x32(col + NP, ml);
+        tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(ml[j]);
+        for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(ml[j]);
+      }
     }
     tc_fence_before();
     __syncwarp();
@@ -272,66 +306,74 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
   }
   // tensor memory is no longer read: let warp 1 free it
   tc_fence_before();
-  asm volatile("bar.arrive 1, 160;" ::: "memory");
+  asm volatile("bar.arrive 1, 288;" ::: "memory");
 
-  const int64_t t = t0 + row;
-  if (!ok) return;   // warp-uniform
-  const bool valid = t < p.T;
-  const int E = p.E;
-
-  // The per-token work below runs once per CTA, so it is written as short
-  // loops over shared-memory rows rather than unrolled register code: the
-  // unrolled form was bound by instruction fetch (each SM meets it cold).
-  // Rows live in the operand ring, idle now (every load landed and every MMA
-  // that read it completed); stride LS = NP + 1 keeps a warp's 32 rows on 32
-  // banks.
-  float* Lrow = reinterpret_cast<float*>(gbase) + row * S::LS;           // logits
-  float* Krow = reinterpret_cast<float*>(gbase) + (128 + row) * S::LS;   // selection keys
+  // The logits rows live in the operand ring, idle now (every load landed and
+  // every MMA that read it completed).
+  float* rows = reinterpret_cast<float*>(gbase);
+  if (ok && drains) {
+    float* Lw = rows + row * S::LS + half * NH;
 #pragma unroll
-  for (int c = 0; c < NP; ++c) Lrow[c] = acc[c];
+    for (int c = 0; c < NH; ++c) Lw[c] = acc[c];
+  }
+  // All eight warps meet here whatever happened: a failed wait set *abort
+  // before its warp got here, so after the barrier every warp sees it.
+  asm volatile("bar.sync 2, 256;" ::: "memory");
+  if (!__all_sync(0xffffffffu, ok && *abort == 0)) return;
+
+  // Two adjacent lanes per token; lane parity hp scans experts c = hp, hp + 2, ...
+  // The per-token work runs once per CTA, so it is written as short loops over
+  // shared-memory rows (unrolled register code was bound by instruction fetch,
+  // each SM meeting it cold).
+  const int tt = threadIdx.x - 64;
+  const int trow = tt >> 1, hp = tt & 1;
+  const int64_t t = t0 + trow;
+  const bool valid = t < p.T;   // the same for both lanes of a pair
+  const int E = p.E;
+  const float* Lrow = rows + trow * S::LS;               // logits
+  float* Krow = rows + (128 + trow) * S::LS;             // selection keys
   if (p.logits_out != nullptr && valid)
-    for (int c = 0; c < E; ++c) p.logits_out[t * E + c] = Lrow[c];
+    for (int c = hp; c < E; c += 2) p.logits_out[t * E + c] = Lrow[c];
   if (p.noise_out != nullptr && valid)
-    for (int c = 0; c < E; ++c) p.noise_out[t * E + c] = Lrow[c + E];
+    for (int c = hp; c < E; c += 2) p.noise_out[t * E + c] = Lrow[c + E];
 
   // softmax over the E gate logits: max, then the sum of exponentials, each
-  // in four interleaved partial chains (element c feeds chain c % 4)
-  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  for (int c = 0; c < E; c += 4) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (c + j < E) mx[j] = fmaxf(mx[j], Lrow[c + j]);
+  // lane over its parity in two interleaved chains, then over the pair
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+  for (int c = hp; c < E; c += 4) {
+    mx0 = fmaxf(mx0, Lrow[c]);
+    if (c + 2 < E) mx1 = fmaxf(mx1, Lrow[c + 2]);
   }
-  const float m = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-  float sm[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = 0; c < E; c += 4) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (c + j < E) sm[j] += expf(Lrow[c + j] - m);
+  float m = fmaxf(mx0, mx1);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  float sm0 = 0.f, sm1 = 0.f;
+  for (int c = hp; c < E; c += 4) {
+    sm0 += expf(Lrow[c] - m);
+    if (c + 2 < E) sm1 += expf(Lrow[c + 2] - m);
   }
-  const float ssum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+  float ssum = sm0 + sm1;
+  ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);   // a + b on one lane, b + a on the other: equal
   const float inv = 1.0f / ssum;
-  if (p.lse != nullptr && valid) p.lse[t] = m + logf(ssum);
+  if (p.lse != nullptr && valid && hp == 0) p.lse[t] = m + logf(ssum);
   if (p.prob_sum != nullptr) {
-    // sum of s over this warp's 32 tokens per expert, then one atomic per warp
-#pragma unroll 4
-    for (int c = 0; c < E; ++c) {
-      float v = valid ? expf(Lrow[c] - m) * inv : 0.f;
+    // sum of s over this warp's 16 tokens per expert, then one atomic per warp
+    for (int c0 = 0; c0 < E; c0 += 2) {
+      const int c = c0 + hp;
+      float v = (valid && c < E) ? expf(Lrow[c] - m) * inv : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) atomicAdd(p.prob_sum + c, v);
+      for (int o = 16; o > 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == hp && c < E) atomicAdd(p.prob_sum + c, v);
     }
   }
-  if (!valid) return;
 
   // selection keys; NaN = not selectable (also the padding up to a multiple of 8)
   const float nan = __int_as_float(0x7fffffff);
   const int E8 = (E + 7) & ~7;   // <= NP
-  for (int c = 0; c < E8; ++c) {
+  for (int c = hp; c < E8; c += 2) {
     float key = nan;
     if (c < E) {
       const float l = Lrow[c];
-      if (p.noisy) key = l + p.eps[t * E + c] * softplus_f(Lrow[c + E]);
+      if (p.noisy) key = l + (valid ? p.eps[t * E + c] : 0.f) * softplus_f(Lrow[c + E]);
       else if (p.bias != nullptr) key = expf(l - m) * inv + __ldg(p.bias + c);
       else key = l;   // Softmax is increasing: the order of s is the order of the logits
       if (key != key) key = -INFINITY;   // a NaN key ranks last, ids stay valid
@@ -339,32 +381,34 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
     Krow[c] = key;
   }
 
-  // k rounds of arg-max: eight chains (chain j scans c = j, j + 8, ... in
-  // increasing order), merged with ties to the lower index; the pick is then
-  // marked taken
+  // k rounds of arg-max: per lane four chains (chain j scans c = hp + 2 j,
+  // hp + 2 j + 8, ... in increasing order), merged with ties to the lower
+  // index, then the pair's two candidates merged the same way (so both lanes
+  // hold the same pick); the lane owning the pick marks it taken
   float sel_sum = 0.f, key0 = 0.f;
   for (int r = 0; r < p.k; ++r) {
-    float kb8[8];
-    int ib8[8];
+    float kb4[4];
+    int ib4[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      kb8[j] = nan;
-      ib8[j] = -1;
+    for (int j = 0; j < 4; ++j) {
+      kb4[j] = nan;
+      ib4[j] = -1;
     }
 #pragma unroll 2
-    for (int c = 0; c < E8; c += 8) {
+    for (int c = hp; c < E8; c += 8) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) argmax_step(Krow[c + j], c + j, kb8[j], ib8[j]);
+      for (int j = 0; j < 4; ++j) argmax_step(Krow[c + 2 * j], c + 2 * j, kb4[j], ib4[j]);
     }
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int j = 0; j < w; ++j) argmax_merge(kb8[j + w], ib8[j + w], kb8[j], ib8[j]);
-    const float kb = kb8[0];
+    argmax_merge(kb4[1], ib4[1], kb4[0], ib4[0]);
+    argmax_merge(kb4[3], ib4[3], kb4[2], ib4[2]);
+    argmax_merge(kb4[2], ib4[2], kb4[0], ib4[0]);
+    float kb = kb4[0];
+    int ib = ib4[0];
+    argmax_merge(__shfl_xor_sync(0xffffffffu, kb, 1), __shfl_xor_sync(0xffffffffu, ib, 1), kb, ib);
     // k <= E and no key below E is NaN, so a selectable entry remains every
     // round; the clamp only keeps the row accesses in bounds regardless
-    const int bi = max(ib8[0], 0);
-    Krow[bi] = nan;
+    const int bi = max(ib, 0);
+    if ((bi & 1) == hp) Krow[bi] = nan;
     float v;
     if (p.noisy) {
       if (r == 0) key0 = kb;
@@ -373,9 +417,12 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
       v = expf(Lrow[bi] - m) * inv;    // s of the pick
     }
     sel_sum += v;
-    p.topk_ids[t * p.k + r] = bi;
-    p.topk_w[t * p.k + r] = v;
+    if (valid && hp == 0) {
+      p.topk_ids[t * p.k + r] = bi;
+      p.topk_w[t * p.k + r] = v;
+    }
   }
+  if (!valid || hp != 0) return;
   if (p.noisy || p.renorm)
     for (int r = 0; r < p.k; ++r) p.topk_w[t * p.k + r] /= sel_sum;
   if (p.gate_sum != nullptr)

@@ -160,6 +160,26 @@ def test_route_tensor_core_odd_shapes(w, cuda_lib):
     test_route(w, cuda_lib)
 
 
+@pytest.mark.parametrize("w", [workloads.DSMOE_145B_DECODE, RAGGED], ids=lambda w: w.name)
+def test_route_k_groups_on_a_dirty_workspace(w, cuda_lib):
+    """Few tokens: k-groups of router clusters meet through the route
+    workspace (partial rows and arrival counters). A workspace full of 0xFF
+    bytes gives the same bits as a fresh one, and so does a second call on it
+    (the counters are cleared per call; the groups are summed in a fixed
+    order)."""
+    inp = get_inputs(w, with_experts=False)
+    cfg = binding.config(w)
+    assert binding.route_workspace_size(cfg) > 0
+    args = (cfg, dev(inp["x"]), dev(inp["W_g"]), dev(inp["W_noise"]), dev(inp["eps"]), dev(inp["bias"]))
+    ids, g, lg = binding.route(*args, want_logits=True)
+    ws = torch.full((binding.route_workspace_size(cfg),), 0xFF, dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        ids2, g2, lg2 = binding.route(*args, want_logits=True, workspace=ws)
+        assert torch.equal(ids, ids2) and torch.equal(g, g2) and torch.equal(lg, lg2)
+    assert binding.device_status()[0] == 0
+    check_routing(w, oracle_route(w, inp), ids, g)
+
+
 @pytest.mark.parametrize("T,E,k", [(70, 64, 6), (4101, 64, 6), (4101, 63, 7), (4101, 20, 3), (4101, 128, 12)])
 def test_route_ties_pick_lowest_index(T, E, k, cuda_lib):
     """All logits equal (W_g = 0): the picks are experts 0..k-1 in order with
