@@ -136,10 +136,9 @@ int moe_version(void);
 
 /* Bytes of scratch moe_route needs. Tensor-core router: the three bf16
  * planes of the router weights. CUDA-core router (fp32 tokens, more than 128
- * router columns, or T < 4096) with T <= 512: partial logits rows and arrival
- * counters of the k-groups that split the reduction over d among more SMs
- * (the counters are cleared by each call, so the scratch needs no
- * initialisation). Otherwise 0. */
+ * router columns, or T < 4096) with T <= 512: the partial logits tiles of the
+ * split of the reduction over d among more SMs (written before they are read:
+ * the scratch needs no initialisation). Otherwise 0. */
 size_t moe_route_workspace_size(const moe_config* cfg);
 
 /*

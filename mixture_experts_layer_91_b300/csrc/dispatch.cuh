@@ -126,6 +126,7 @@ __device__ void plan_groups(const int32_t* offsets, int32_t E, int32_t K_s, int6
 }
 
 constexpr int kScanThreads = 1024;
+constexpr int kScanStageInts = 8192;   // 32 KB of per-block counts staged in shared memory
 
 // One CTA. blk_hist [nblk][E]: per-block counts in, per-block rank bases out
 // (the assignments of expert e in earlier blocks). counts/offsets are the
@@ -139,6 +140,20 @@ __global__ void __launch_bounds__(kScanThreads)
   pdl_launch_dependents();
   __shared__ int32_t tot[kMaxGroups + 1];
   __shared__ int32_t part[kScanThreads];
+  // The histogram staged in shared memory when it fits (the headline-sized
+  // layers): one round of independent coalesced loads, where the walks below
+  // over global memory would wait a load latency per block.
+  __shared__ int32_t hs[kScanStageInts];
+  const int64_t nh = static_cast<int64_t>(nblk) * E;
+  const bool staged = nh <= kScanStageInts;
+  if (staged) {
+#pragma unroll
+    for (int j = 0; j < kScanStageInts / kScanThreads; ++j) {
+      const int i = threadIdx.x + j * kScanThreads;
+      if (i < nh) hs[i] = blk_hist[i];
+    }
+    __syncthreads();
+  }
   // split the block range of each expert over `parts` threads
   const int parts = max(1, kScanThreads / E);
   const int e = threadIdx.x % E;
@@ -148,7 +163,10 @@ __global__ void __launch_bounds__(kScanThreads)
   const int b0 = pi * span, b1 = min(nblk, b0 + span);
   int32_t run = 0;
   if (active)
-    for (int b = b0; b < b1; ++b) run += blk_hist[static_cast<int64_t>(b) * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const int64_t i = static_cast<int64_t>(b) * E + e;
+      run += staged ? hs[i] : blk_hist[i];
+    }
   part[threadIdx.x] = active ? run : 0;
   __syncthreads();
   if (threadIdx.x < E) {
@@ -173,7 +191,7 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int j = 0; j < pi; ++j) base += part[j * E + e];
     for (int b = b0; b < b1; ++b) {
       const int64_t i = static_cast<int64_t>(b) * E + e;
-      const int32_t v = blk_hist[i];
+      const int32_t v = staged ? hs[i] : blk_hist[i];
       blk_hist[i] = base;
       base += v;
     }

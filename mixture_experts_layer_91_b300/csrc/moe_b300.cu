@@ -84,11 +84,11 @@ size_t router_planes_bytes(const moe_config* c) {
   return static_cast<size_t>(3) * router_tc_np(c) * c->d * 2;
 }
 
-// The CUDA-core router's k-groups (RouterArgs::kgroups): at most 16, and only
-// for T <= 512 (16 token blocks), where one cluster per token block leaves
-// most SMs idle.
-constexpr int kRouterMaxGroups = 16;
-constexpr int64_t kRouterGroupMaxTokens = 512;
+// The CUDA-core router's split-K form (router_partial_kernel +
+// router_finish_kernel): only for T <= 512 (16 token blocks), where one CTA
+// or cluster per token block leaves most SMs idle; at most 32 splits.
+constexpr int kRouterMaxSplits = 32;
+constexpr int64_t kRouterSplitMaxTokens = 512;
 constexpr int kRouterMaxCluster = 8;
 
 int router_epad(const moe_config* c) {
@@ -96,24 +96,23 @@ int router_epad(const moe_config* c) {
   return cols <= 32 ? 32 : (cols <= 64 ? 64 : (cols <= 128 ? 128 : 256));
 }
 
-// Bytes of the k-groups' partial rows ([block][group][32][EPAD] fp32) and
-// arrival counters ([block][cluster rank] int32); 0 where no k-groups run.
-size_t router_group_part_bytes(const moe_config* c) {
-  if (router_tc_np(c) > 0 || c->T == 0 || c->T > kRouterGroupMaxTokens) return 0;
-  const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
-  return (static_cast<size_t>(nblk) * kRouterMaxGroups * kRouterBT * router_epad(c) * 4 + 255) &
-         ~static_cast<size_t>(255);
-}
+// Bytes of the split-K partial logits tiles ([block][split][32][EPAD] fp32);
+// 0 where the split-K form does not run.
 size_t router_group_bytes(const moe_config* c) {
-  const size_t part = router_group_part_bytes(c);
-  if (part == 0) return 0;
+  if (router_tc_np(c) > 0 || c->T == 0 || c->T > kRouterSplitMaxTokens) return 0;
   const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
-  return part + static_cast<size_t>(nblk) * kRouterMaxCluster * 4;
+  return static_cast<size_t>(nblk) * kRouterMaxSplits * kRouterBT * router_epad(c) * 4;
 }
 
-// Scratch of launch_route: the planes (tensor-core router) or the k-groups'
-// rows and counters (CUDA-core router, few tokens); at most one is non-zero.
-size_t router_scratch_bytes(const moe_config* c) { return router_planes_bytes(c) + router_group_bytes(c); }
+// Scratch of launch_route. Tensor-core router: the planes, then its fp32
+// logits rows [T][NP] for the finish kernel. CUDA-core router with few tokens:
+// the split-K partial tiles. Otherwise nothing.
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+size_t router_scratch_bytes(const moe_config* c) {
+  const int np = router_tc_np(c);
+  if (np > 0) return align256(router_planes_bytes(c)) + align256(static_cast<size_t>(c->T) * np * 4);
+  return router_group_bytes(c);
+}
 
 // ---------------------------------------------------------------------------
 // workspace layouts (every region 256-byte aligned)
@@ -327,6 +326,9 @@ moe_status device_state(DeviceState** out) {
 #undef MOE_RTC_ATTR
 #define MOE_ROUTER_ATTR(TX, EP)                                                                  \
   ok &= cudaFuncSetAttribute(router_kernel<TX, EP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             static_cast<int>(router_smem_bytes<EP>())) == cudaSuccess;          \
+  ok &= cudaFuncSetAttribute(router_partial_kernel<TX, EP>,                                      \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,                        \
                              static_cast<int>(router_smem_bytes<EP>())) == cudaSuccess;
     MOE_ROUTER_ATTR(float, 32) MOE_ROUTER_ATTR(float, 64) MOE_ROUTER_ATTR(float, 128)
     MOE_ROUTER_ATTR(float, 256) MOE_ROUTER_ATTR(__nv_bfloat16, 32)
@@ -447,8 +449,6 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   a.prob_sum = stats ? stats->prob_sum : nullptr;
   a.gate_sum = stats ? stats->gate_sum : nullptr;
   a.part = nullptr;
-  a.part_count = nullptr;
-  a.kgroups = 1;
   if (c->T > 0) {   // the per-expert sums are accumulated with atomics
     if (a.prob_sum && cudaMemsetAsync(a.prob_sum, 0, sizeof(float) * c->n_routed, st) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -461,6 +461,7 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
     if (c->T == 0) return MOE_OK;
     // split [W_g | W_noise] into three bf16 planes, then the tensor-core router
     auto* pl = static_cast<__nv_bfloat16*>(scratch);
+    a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align256(router_planes_bytes(c)));
     router_split_kernel<<<dim3(static_cast<unsigned>((c->d + 31) / 32), static_cast<unsigned>(np / 32)), 256, 0,
                           st>>>(W_g, W_noise, c->d, c->n_routed, cols, np, pl);
     MOE_TRY(last_launch());
@@ -495,32 +496,55 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
       cudaGetLastError();
       return MOE_ERR_CUDA;
     }
-    return last_launch();
+    MOE_TRY(last_launch());
+    // softmax, keys, top-k and gates per token: the finish kernel over the
+    // logits rows as the one split of its layout
+    // (NP / 8 lanes per token, as many tokens as fill a CTA)
+    const int32_t tpc = kRouterFinishThreads * 8 / np;
+    const dim3 fgrid(static_cast<unsigned>((c->T + tpc - 1) / tpc));
+    const dim3 fblock(kRouterFinishThreads);
+    if (np == 32) return launch_dependent(router_finish_kernel<32>, fgrid, fblock, 0, st, a, 1, tpc);
+    if (np == 64) return launch_dependent(router_finish_kernel<64>, fgrid, fblock, 0, st, a, 1, tpc);
+    return launch_dependent(router_finish_kernel<128>, fgrid, fblock, 0, st, a, 1, tpc);
   }
   const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
   if (nblk == 0) return MOE_OK;
-  // Few token blocks (decode-sized T): a cluster of CS CTAs also splits the
-  // k-chunks, until there are about two CTAs per SM or two chunks per CTA.
   const int nchunk = (c->d + 63) / 64;   // the smallest k-chunk of any router shape
+  const bool bf = c->act_dtype == MOE_DT_BF16;
+  cudaError_t e;
+  // Few tokens (T <= 512): split-K over independent CTAs, about one per SM,
+  // then the finish kernel (a programmatic dependent) per 8 tokens.
+  const int64_t nsplit = std::min<int64_t>(std::min<int64_t>(nchunk, kRouterMaxSplits), sm_count / nblk);
+  if (router_group_bytes(c) > 0 && nsplit >= 2) {
+    a.part = static_cast<float*>(scratch);
+    const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>(nsplit));
+    // the finish kernel: enough tokens per CTA for an element per thread, or
+    // about one CTA per SM if that takes more (at most 256 / (EPAD / 8))
+    const int32_t ns = static_cast<int32_t>(nsplit);
+    const int64_t ep = router_epad(c);
+    const int32_t tpc = static_cast<int32_t>(std::min<int64_t>(
+        kRouterFinishThreads * 8 / ep,
+        std::max<int64_t>((kRouterFinishThreads + ep - 1) / ep, (c->T + sm_count - 1) / sm_count)));
+    const dim3 fgrid(static_cast<unsigned>((c->T + tpc - 1) / tpc));
+    const dim3 fblock(kRouterFinishThreads);
+#define MOE_ROUTE_SPLIT(EP)                                                                                   \
+  if (bf) router_partial_kernel<__nv_bfloat16, EP><<<grid, kRouterThreads, router_smem_bytes<EP>(), st>>>(a); \
+  else router_partial_kernel<float, EP><<<grid, kRouterThreads, router_smem_bytes<EP>(), st>>>(a);           \
+  MOE_TRY(last_launch());                                                                                     \
+  return launch_dependent(router_finish_kernel<EP>, fgrid, fblock, 0, st, a, ns, tpc);
+    if (cols <= 32) { MOE_ROUTE_SPLIT(32) }
+    else if (cols <= 64) { MOE_ROUTE_SPLIT(64) }
+    else if (cols <= 128) { MOE_ROUTE_SPLIT(128) }
+    else { MOE_ROUTE_SPLIT(256) }
+#undef MOE_ROUTE_SPLIT
+  }
+  // Otherwise, with few token blocks a cluster of CS CTAs also splits the
+  // k-chunks, until there are about two CTAs per SM or two chunks per CTA.
   int cs = 1;
   while (cs < kRouterMaxCluster && nblk * cs < 2ll * sm_count && nchunk >= 4 * cs) cs *= 2;
-  // Still far fewer CTAs than SMs (T <= 512): k-groups of clusters, until
-  // about one CTA per SM or one chunk per CTA.
-  int kg = 1;
-  if (router_group_bytes(c) > 0)
-    while (2 * kg <= kRouterMaxGroups && nblk * cs * 2 * kg <= sm_count && nchunk >= cs * 2 * kg) kg *= 2;
-  if (kg > 1) {
-    a.kgroups = kg;
-    a.part = static_cast<float*>(scratch);
-    a.part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + router_group_part_bytes(c));
-    if (cudaMemsetAsync(a.part_count, 0, sizeof(int32_t) * nblk * cs, st) != cudaSuccess) {
-      cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
-  }
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[1];
-  lc.gridDim = dim3(static_cast<unsigned>(nblk * kg * cs), 1, 1);
+  lc.gridDim = dim3(static_cast<unsigned>(nblk * cs), 1, 1);
   lc.blockDim = dim3(kRouterThreads, 1, 1);
   lc.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -529,8 +553,6 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  const bool bf = c->act_dtype == MOE_DT_BF16;
-  cudaError_t e;
 #define MOE_ROUTE(EP)                                                                \
   lc.dynamicSmemBytes = router_smem_bytes<EP>();                                     \
   e = bf ? cudaLaunchKernelEx(&lc, router_kernel<__nv_bfloat16, EP>, a)              \

@@ -20,11 +20,10 @@
 // memory in a fixed order. When T is small a thread-block cluster of CS CTAs
 // also splits the k-chunks; each CTA of the cluster then owns BT / CS of the
 // tokens and adds their partial rows from every CTA's tile through
-// distributed shared memory (ranks in order). With very few tokens, k-groups
-// of such clusters split the chunks further: each writes its rows to global
-// scratch, and the last group to arrive for a token share sums them in group
-// order. Per token, one warp computes the softmax and a k-round warp arg-max
-// (ties to the lower index).
+// distributed shared memory (ranks in order). With very few tokens (T <= 512)
+// a grid of independent CTAs splits the chunks instead, and a second kernel
+// sums each token's partial rows in split order. Per token, one warp computes
+// the softmax and a k-round warp arg-max (ties to the lower index).
 #pragma once
 
 #include "common.cuh"
@@ -50,15 +49,8 @@ struct RouterArgs {
   float* lse;
   float* prob_sum;
   float* gate_sum;
-  // k-groups (CUDA-core router, few tokens): kgroups clusters share one token
-  // block, each over every kgroups-th run of k-chunks; their partial logits
-  // rows meet in `part` ([block][group][BT][EPAD] fp32), and per token share
-  // (block, cluster rank) an arrival counter `part_count` (zero at launch)
-  // picks the last group to arrive, which sums the groups in group order and
-  // finishes those tokens. kgroups = 1: no k-groups.
+  // split-K partial logits tiles (router_partial_kernel -> router_finish_kernel)
   float* part;
-  int32_t* part_count;
-  int32_t kgroups;
 };
 
 constexpr int kRouterBT = 32;       // tokens per CTA
@@ -298,57 +290,29 @@ __device__ __forceinline__ void router_mainloop(const RouterArgs& p, float* rsm,
   __syncthreads();
 }
 
+// The CTA's logits tile over its chunks (first, first + step, ...): the
+// register tiles of the k-phases summed in a fixed order into rows
+// rsm[token * LS + column] (rows of the CTA's BT tokens, EPAD columns).
 template <typename TX, int EPAD>
-__global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_kernel(const RouterArgs p) {
+__device__ __forceinline__ void router_block_logits(const RouterArgs& p, float* rsm, int64_t t0, int first,
+                                                    int step) {
   using S = RouterShape<EPAD>;
   constexpr int TM = S::TM, TN = S::TN;
-  extern __shared__ __align__(16) float rsm[];
-
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int tg = lane >> 3, cg = lane & 7;          // token group, column group of this lane
-  pdl_launch_dependents();   // the dispatch kernels may launch and wait for this one
   const int wr = warp / S::SPLIT;                   // warp row
   const int ks = warp % S::SPLIT;                   // k-step phase of this warp inside a chunk
   const int tok0 = wr * S::WT + tg * TM;            // first token (CTA-local) of the thread tile
-
-  const uint32_t crank = cluster_rank();
-  const uint32_t csize = cluster_size();
-  const int64_t cid = blockIdx.x / csize;                  // cluster
-  const int kg = static_cast<int>(cid % p.kgroups);       // its k-group
-  const int64_t tb = cid / p.kgroups;                     // its token block
-  const int64_t t0 = tb * S::BT;
-  __shared__ float s_prob[EPAD], s_gate[EPAD];   // per-CTA statistic sums
-  for (int c = tid; c < EPAD; c += kRouterThreads) {
-    s_prob[c] = 0.f;
-    s_gate[c] = 0.f;
-  }
-
-  // fused clear of the fp32 accumulator rows of these tokens (forward path),
-  // shared among the CTAs of the cluster
-  if (p.zero_rows != nullptr && kg == 0) {
-    const int64_t rows = (p.T - t0 < S::BT) ? (p.T - t0) : S::BT;
-    float4* z = reinterpret_cast<float4*>(p.zero_rows + t0 * p.zero_width);
-    const int64_t n4 = rows * p.zero_width / 4;
-    for (int64_t i = tid + static_cast<int64_t>(crank) * kRouterThreads; i < n4;
-         i += static_cast<int64_t>(kRouterThreads) * csize)
-      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
   float acc[TM][TN];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-  // chunks kg * csize + crank, then every (kgroups * csize)-th
-  const int first = kg * static_cast<int>(csize) + static_cast<int>(crank);
-  const int step = p.kgroups * static_cast<int>(csize);
   if (p.w_vec4)
     router_mainloop<TX, EPAD, 4>(p, rsm, t0, first, step, tid, tok0, ks, cg, acc);
   else
     router_mainloop<TX, EPAD, 1>(p, rsm, t0, first, step, tid, tok0, ks, cg, acc);
-
   // partial tiles of the k-phases: part[ks][token][column]
   float* part = rsm;
 #pragma unroll
@@ -366,6 +330,142 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
     part[tok * S::LS + col] = s;
   }
   __syncthreads();
+}
+
+// Softmax, keys, top-k and gates of token t from its logits row Lr (EPAD
+// columns: the N_r gate logits, then the noise logits when noisy); one warp.
+// The per-expert statistic sums go to the CTA's s_prob / s_gate.
+template <int EPAD>
+__device__ __forceinline__ void router_token(const RouterArgs& p, const float* Lr, int64_t t, int lane,
+                                             float* s_prob, float* s_gate) {
+  constexpr int PER_LANE = EPAD / 32;
+  float lg[PER_LANE], key[PER_LANE], sv[PER_LANE];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int cc = lane + 32 * i;
+    lg[i] = (cc < p.E) ? Lr[cc] : -INFINITY;
+    m = fmaxf(m, lg[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float ssum = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int cc = lane + 32 * i;
+    sv[i] = (cc < p.E) ? expf(lg[i] - m) : 0.f;
+    ssum += sv[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+  const float inv = 1.0f / ssum;
+  if (p.lse != nullptr && lane == 0) p.lse[t] = m + logf(ssum);
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int cc = lane + 32 * i;
+    sv[i] *= inv;
+    if (p.prob_sum != nullptr && cc < p.E) atomicAdd(&s_prob[cc], sv[i]);
+    if (cc >= p.E) {
+      key[i] = -INFINITY;
+    } else if (p.noisy) {
+      key[i] = lg[i] + p.eps[t * p.E + cc] * softplus_f(Lr[p.E + cc]);
+    } else if (p.bias != nullptr) {
+      key[i] = sv[i] + p.bias[cc];
+    } else {
+      key[i] = lg[i];   // Softmax is increasing: the order of s is the order of the logits
+    }
+    if (key[i] != key[i]) key[i] = -INFINITY;   // a NaN key ranks last, ids stay valid
+    if (p.logits_out != nullptr && cc < p.E) p.logits_out[t * p.E + cc] = lg[i];
+    if (p.noise_out != nullptr && cc < p.E) p.noise_out[t * p.E + cc] = Lr[p.E + cc];
+  }
+
+  uint32_t taken = 0;
+  int my_id = 0;
+  float my_val = 0.f;   // s of the pick (softmax gate) or its key H (noisy)
+  float sel_sum = 0.f, key0 = 0.f;
+  for (int r = 0; r < p.k; ++r) {
+    float kb = -INFINITY, vb = 0.f;
+    int ib = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      const int cc = lane + 32 * i;
+      if (cc < p.E && !((taken >> i) & 1u) && better(key[i], cc, kb, ib)) {
+        kb = key[i];
+        ib = cc;
+        vb = p.noisy ? key[i] : sv[i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ko = __shfl_xor_sync(0xffffffffu, kb, o);
+      const int io = __shfl_xor_sync(0xffffffffu, ib, o);
+      const float vo = __shfl_xor_sync(0xffffffffu, vb, o);
+      if (better(ko, io, kb, ib)) {
+        kb = ko;
+        ib = io;
+        vb = vo;
+      }
+    }
+    if ((ib & 31) == lane) taken |= 1u << (ib >> 5);
+    if (r == 0) key0 = vb;
+    if (p.noisy) vb = expf(vb - key0);   // softmax over the kept H (max is the first pick)
+    sel_sum += vb;
+    if (lane == r) {
+      my_id = ib;
+      my_val = vb;
+    }
+  }
+  if (lane < p.k) {
+    float g = my_val;
+    if (p.noisy || p.renorm) g = my_val / sel_sum;
+    p.topk_ids[t * p.k + lane] = my_id;
+    p.topk_w[t * p.k + lane] = g;
+    if (p.gate_sum != nullptr) atomicAdd(&s_gate[my_id], g);
+  }
+}
+
+// The CTA's statistic sums into the per-expert totals (after a __syncthreads).
+template <int EPAD>
+__device__ __forceinline__ void router_flush_stats(const RouterArgs& p, const float* s_prob, const float* s_gate) {
+  if (p.prob_sum == nullptr && p.gate_sum == nullptr) return;
+  for (int c = threadIdx.x; c < p.E; c += blockDim.x) {
+    if (p.prob_sum != nullptr) atomicAdd(p.prob_sum + c, s_prob[c]);
+    if (p.gate_sum != nullptr) atomicAdd(p.gate_sum + c, s_gate[c]);
+  }
+}
+
+// Fused clear of the fp32 accumulator rows [t_begin, t_end) (forward path),
+// threads `first`, `first + stride`, ... of the launch taking 16-byte pieces.
+__device__ __forceinline__ void router_zero_rows(const RouterArgs& p, int64_t t_begin, int64_t t_end,
+                                                 int64_t first, int64_t stride) {
+  if (p.zero_rows == nullptr || t_end <= t_begin) return;
+  float4* z = reinterpret_cast<float4*>(p.zero_rows + t_begin * p.zero_width);
+  const int64_t n4 = (t_end - t_begin) * p.zero_width / 4;
+  for (int64_t i = first; i < n4; i += stride) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One CTA per BT tokens; a cluster of CS CTAs (CS >= 1) splits the chunks and
+// each CTA finishes BT / CS of the tokens.
+template <typename TX, int EPAD>
+__global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_kernel(const RouterArgs p) {
+  using S = RouterShape<EPAD>;
+  extern __shared__ __align__(16) float rsm[];
+  pdl_launch_dependents();   // the dispatch kernels may launch and wait for this one
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_rank();
+  const uint32_t csize = cluster_size();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * S::BT;
+  __shared__ float s_prob[EPAD], s_gate[EPAD];   // per-CTA statistic sums
+  for (int c = tid; c < EPAD; c += kRouterThreads) {
+    s_prob[c] = 0.f;
+    s_gate[c] = 0.f;
+  }
+  // the clear of the tokens' fp32 accumulator rows is shared among the cluster
+  router_zero_rows(p, t0, (p.T - t0 < S::BT) ? p.T : t0 + S::BT, tid + static_cast<int64_t>(crank) * kRouterThreads,
+                   static_cast<int64_t>(kRouterThreads) * csize);
+  router_block_logits<TX, EPAD>(p, rsm, t0, static_cast<int>(crank), static_cast<int>(csize));
+  float* part = rsm;
   // Tokens this CTA finishes: all of the tile, or with a cluster its rank's
   // share (BT / csize consecutive tokens).
   int tok_begin = 0, tok_end = S::BT;
@@ -393,134 +493,189 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
     }
     cluster_sync_all();   // no CTA leaves while another still reads its tile
   }
-  if (p.kgroups > 1) {
-    // This group's rows of the share go to the scratch; the last group to
-    // arrive sums every group's rows in group order (a fixed summation order
-    // whatever the arrival order) and finishes the share's tokens.
-    const int share = tok_end - tok_begin;
-    const int64_t blk0 = tb * p.kgroups * S::BT * EPAD;   // the block's first group row
-    float* mine = p.part + blk0 + static_cast<int64_t>(kg) * S::BT * EPAD;
-    for (int idx = tid; idx < share * EPAD; idx += kRouterThreads) {
-      const int tok = tok_begin + idx / EPAD, col = idx % EPAD;
-      mine[tok * EPAD + col] = part[tok * S::LS + col];
-    }
-    __threadfence();
-    __syncthreads();
-    __shared__ int s_last;
-    int32_t* cnt = p.part_count + tb * csize + crank;
-    if (tid == 0) s_last = atomicAdd(cnt, 1) == p.kgroups - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const float* all = p.part + blk0;
-    for (int idx = tid; idx < share * EPAD; idx += kRouterThreads) {
-      const int tok = tok_begin + idx / EPAD, col = idx % EPAD;
-      float s = __ldcg(all + tok * EPAD + col);
-      for (int g = 1; g < p.kgroups; ++g) s += __ldcg(all + (static_cast<int64_t>(g) * S::BT + tok) * EPAD + col);
-      part[tok * S::LS + col] = s;
-    }
-    if (tid == 0) *cnt = 0;   // every group has arrived: ready for the next launch
-    __syncthreads();
-  }
-
   // per-token softmax + top-k: one warp per token
-  constexpr int PER_LANE = EPAD / 32;
-  const float* L = part;
   for (int tok = tok_begin + warp; tok < tok_end; tok += kRouterWarps) {
     const int64_t t = t0 + tok;
     if (t >= p.T) break;
-    const float* Lr = L + tok * S::LS;
-    float lg[PER_LANE], key[PER_LANE], sv[PER_LANE];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int cc = lane + 32 * i;
-      lg[i] = (cc < p.E) ? Lr[cc] : -INFINITY;
-      m = fmaxf(m, lg[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float ssum = 0.f;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int cc = lane + 32 * i;
-      sv[i] = (cc < p.E) ? expf(lg[i] - m) : 0.f;
-      ssum += sv[i];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-    const float inv = 1.0f / ssum;
-    if (p.lse != nullptr && lane == 0) p.lse[t] = m + logf(ssum);
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int cc = lane + 32 * i;
-      sv[i] *= inv;
-      if (p.prob_sum != nullptr && cc < p.E) atomicAdd(&s_prob[cc], sv[i]);
-      if (cc >= p.E) {
-        key[i] = -INFINITY;
-      } else if (p.noisy) {
-        key[i] = lg[i] + p.eps[t * p.E + cc] * softplus_f(Lr[p.E + cc]);
-      } else if (p.bias != nullptr) {
-        key[i] = sv[i] + p.bias[cc];
-      } else {
-        key[i] = lg[i];   // Softmax is increasing: the order of s is the order of the logits
-      }
-      if (key[i] != key[i]) key[i] = -INFINITY;   // a NaN key ranks last, ids stay valid
-      if (p.logits_out != nullptr && cc < p.E) p.logits_out[t * p.E + cc] = lg[i];
-      if (p.noise_out != nullptr && cc < p.E) p.noise_out[t * p.E + cc] = Lr[p.E + cc];
-    }
+    router_token<EPAD>(p, part + tok * S::LS, t, lane, s_prob, s_gate);
+  }
+  __syncthreads();
+  router_flush_stats<EPAD>(p, s_prob, s_gate);
+}
 
-    uint32_t taken = 0;
-    int my_id = 0;
-    float my_val = 0.f;   // s of the pick (softmax gate) or its key H (noisy)
-    float sel_sum = 0.f, key0 = 0.f;
-    for (int r = 0; r < p.k; ++r) {
-      float kb = -INFINITY, vb = 0.f;
-      int ib = 0x7fffffff;
+// Few tokens (T <= 512): split-K over a grid (token blocks, S) of independent
+// CTAs (no clusters: their placement costs microseconds at this size). CTA
+// (b, s) writes its partial logits tile over chunks s, s + S, ... to
+// part[b][s][BT][EPAD]; router_finish_kernel sums the S tiles of a token in
+// order s = 0, 1, ... and finishes it. (The tensor-core router writes its
+// logits as the one split of this layout: [T][EPAD].)
+template <typename TX, int EPAD>
+__global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_partial_kernel(const RouterArgs p) {
+  using S = RouterShape<EPAD>;
+  extern __shared__ __align__(16) float rsm[];
+  pdl_launch_dependents();   // the finish kernel may launch and wait for this one
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * S::BT;
+  router_block_logits<TX, EPAD>(p, rsm, t0, static_cast<int>(blockIdx.y), static_cast<int>(gridDim.y));
+  float* out = p.part + (static_cast<int64_t>(blockIdx.x) * gridDim.y + blockIdx.y) * S::BT * EPAD;
+  for (int idx = threadIdx.x; idx < S::BT * EPAD / 4; idx += kRouterThreads) {
+    const int tok = idx / (EPAD / 4), col = 4 * (idx % (EPAD / 4));
+    const float* r = rsm + tok * S::LS + col;
+    reinterpret_cast<float4*>(out)[idx] = make_float4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+// router_finish_kernel: G = EPAD / 8 lanes per token, each over 8 contiguous
+// experts (c = 8 sub + j). A CTA of 256 threads takes tpc <= 256 / G tokens:
+// first all its threads add the tokens' split partial rows in split order
+// into shared rows, then each G-lane group runs its token's softmax, keys and
+// k arg-max rounds (a scan of the lane's 8 entries, then xor shuffles inside
+// the group; larger key, or on equal keys the lower expert index).
+constexpr int kRouterFinishThreads = 256;
+constexpr int kRouterMaxTopK = 32;   // the largest k a layer may select
+
+template <int EPAD>
+__global__ void __launch_bounds__(kRouterFinishThreads) router_finish_kernel(const RouterArgs p, int32_t nsplit,
+                                                                             int32_t tpc) {
+  constexpr int G = EPAD / 8;                       // lanes per token
+  constexpr int MAXT = kRouterFinishThreads / G;    // tokens per CTA at most
+  pdl_wait();   // the logits (partial) rows are complete and visible from here on
+  pdl_launch_dependents();
+  __shared__ float rows[MAXT][EPAD + 1];
+  __shared__ float s_prob[EPAD], s_gate[EPAD];
+  __shared__ int32_t s_pick[MAXT][kRouterMaxTopK];   // each token's picks and gates,
+  __shared__ float s_val[MAXT][kRouterMaxTopK];      // written to HBM once at the end
+  const int tid = threadIdx.x;
+  for (int c = tid; c < EPAD; c += kRouterFinishThreads) {
+    s_prob[c] = 0.f;
+    s_gate[c] = 0.f;
+  }
+  const int64_t tb0 = static_cast<int64_t>(blockIdx.x) * tpc;
+  const int64_t tb1 = (p.T - tb0 < tpc) ? p.T : tb0 + tpc;
+  router_zero_rows(p, tb0, tb1, tid, kRouterFinishThreads);
+  // 1. the tokens' logits rows: the partial rows added in split order. Thread
+  // i takes elements i, i + 256, ... (at most MAXT * EPAD / 256 = 8); the
+  // loads of all its elements, and of 16 splits at a time, go out before the
+  // adds that need them.
+  constexpr int64_t kStride = static_cast<int64_t>(kRouterBT) * EPAD;   // between splits
+  constexpr int J = MAXT * EPAD / kRouterFinishThreads;
+  static_assert(J * kRouterFinishThreads == MAXT * EPAD, "finish elements");
+  const int nel = tpc * EPAD;
+  const float* src[J];
+  float acc[J];
 #pragma unroll
-      for (int i = 0; i < PER_LANE; ++i) {
-        const int cc = lane + 32 * i;
-        if (cc < p.E && !((taken >> i) & 1u) && better(key[i], cc, kb, ib)) {
-          kb = key[i];
-          ib = cc;
-          vb = p.noisy ? key[i] : sv[i];
-        }
-      }
+  for (int j = 0; j < J; ++j) {
+    const int e = tid + kRouterFinishThreads * j;
+    const int64_t t = tb0 + e / EPAD;
+    const bool in = e < nel && t < p.T;
+    src[j] = in ? p.part + ((t / kRouterBT) * nsplit * kRouterBT + t % kRouterBT) * EPAD + e % EPAD : nullptr;
+    acc[j] = in ? __ldg(src[j]) : 0.f;
+  }
+#pragma unroll 16
+  for (int q = 1; q < nsplit; ++q)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ko = __shfl_xor_sync(0xffffffffu, kb, o);
-        const int io = __shfl_xor_sync(0xffffffffu, ib, o);
-        const float vo = __shfl_xor_sync(0xffffffffu, vb, o);
-        if (better(ko, io, kb, ib)) {
-          kb = ko;
-          ib = io;
-          vb = vo;
-        }
-      }
-      if ((ib & 31) == lane) taken |= 1u << (ib >> 5);
-      if (r == 0) key0 = vb;
-      if (p.noisy) vb = expf(vb - key0);   // softmax over the kept H (max is the first pick)
-      sel_sum += vb;
-      if (lane == r) {
-        my_id = ib;
-        my_val = vb;
+    for (int j = 0; j < J; ++j)
+      if (src[j] != nullptr) acc[j] += __ldg(src[j] + q * kStride);
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int e = tid + kRouterFinishThreads * j;
+    if (e < nel) rows[e / EPAD][e % EPAD] = acc[j];
+  }
+  __syncthreads();
+
+  // 2. per token, G lanes (every warp runs the loop shape; lanes of tokens
+  // past tpc or T compute on whatever the row holds and write nothing)
+  const int tok = tid / G, sub = tid % G;
+  const int64_t t = tb0 + tok;
+  const bool valid = tok < tpc && t < p.T;
+  const int E = p.E;
+  const float* Lr = rows[tok];
+  float lg[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c = 8 * sub + j;
+    lg[j] = c < E ? Lr[c] : -INFINITY;
+  }
+  float m = lg[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) m = fmaxf(m, lg[j]);
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float ssum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (8 * sub + j < E) ssum += expf(lg[j] - m);
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+  const float inv = 1.0f / ssum;
+  if (valid && sub == 0 && p.lse != nullptr) p.lse[t] = m + logf(ssum);
+  float key[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c = 8 * sub + j;
+    float kf = -INFINITY;
+    if (c < E) {
+      if (valid && p.prob_sum != nullptr) atomicAdd(&s_prob[c], expf(lg[j] - m) * inv);
+      if (p.noisy) kf = lg[j] + (valid ? p.eps[t * E + c] : 0.f) * softplus_f(Lr[E + c]);
+      else if (p.bias != nullptr) kf = expf(lg[j] - m) * inv + __ldg(p.bias + c);
+      else kf = lg[j];   // Softmax is increasing: the order of s is the order of the logits
+      if (kf != kf) kf = -INFINITY;   // a NaN key ranks last, ids stay valid
+      if (valid && p.logits_out != nullptr) p.logits_out[t * E + c] = lg[j];
+      if (valid && p.noise_out != nullptr) p.noise_out[t * E + c] = Lr[E + c];
+    }
+    key[j] = kf;
+  }
+  uint32_t taken = 0;   // bit j: entry j picked already
+  float sel_sum = 0.f, key0 = 0.f;
+  for (int r = 0; r < p.k; ++r) {
+    float kb = -INFINITY;
+    int ib = 0x7fffffff;   // no untaken entry: loses to any real one
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = 8 * sub + j;
+      if (c < E && !((taken >> j) & 1u) && (key[j] > kb || ib == 0x7fffffff)) {
+        kb = key[j];
+        ib = c;
       }
     }
-    if (lane < p.k) {
-      float g = my_val;
-      if (p.noisy || p.renorm) g = my_val / sel_sum;
-      p.topk_ids[t * p.k + lane] = my_id;
-      p.topk_w[t * p.k + lane] = g;
-      if (p.gate_sum != nullptr) atomicAdd(&s_gate[my_id], g);
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+      const float ko = __shfl_xor_sync(0xffffffffu, kb, o);
+      const int io = __shfl_xor_sync(0xffffffffu, ib, o);
+      if (better(ko, io, kb, ib)) {
+        kb = ko;
+        ib = io;
+      }
+    }
+    // k <= E leaves an untaken entry every round; the clamp only keeps the
+    // row access in bounds regardless
+    const int bi = min(max(ib, 0), EPAD - 1);
+    if (bi / 8 == sub) taken |= 1u << (bi % 8);
+    float v;
+    if (p.noisy) {
+      if (r == 0) key0 = kb;
+      v = expf(kb - key0);            // softmax over the kept H (max is the first pick)
+    } else {
+      v = expf(Lr[bi] - m) * inv;     // s of the pick
+    }
+    sel_sum += v;
+    if (sub == 0) {
+      s_pick[tok][r] = bi;
+      s_val[tok][r] = v;
     }
   }
-  if (p.prob_sum != nullptr || p.gate_sum != nullptr) {
-    __syncthreads();
-    for (int c = tid; c < p.E; c += kRouterThreads) {
-      if (p.prob_sum != nullptr) atomicAdd(p.prob_sum + c, s_prob[c]);
-      if (p.gate_sum != nullptr) atomicAdd(p.gate_sum + c, s_gate[c]);
+  __syncwarp();   // a token's G lanes share one warp
+  if (valid) {
+    for (int r = sub; r < p.k; r += G) {
+      const int32_t id = s_pick[tok][r];
+      float g = s_val[tok][r];
+      if (p.noisy || p.renorm) g /= sel_sum;
+      p.topk_ids[t * p.k + r] = id;
+      p.topk_w[t * p.k + r] = g;
+      if (p.gate_sum != nullptr) atomicAdd(&s_gate[id], g);
     }
   }
+  __syncthreads();
+  router_flush_stats<EPAD>(p, s_prob, s_gate);
 }
 
 }  // namespace moe

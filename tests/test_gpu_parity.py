@@ -161,12 +161,11 @@ def test_route_tensor_core_odd_shapes(w, cuda_lib):
 
 
 @pytest.mark.parametrize("w", [workloads.DSMOE_145B_DECODE, RAGGED], ids=lambda w: w.name)
-def test_route_k_groups_on_a_dirty_workspace(w, cuda_lib):
-    """Few tokens: k-groups of router clusters meet through the route
-    workspace (partial rows and arrival counters). A workspace full of 0xFF
-    bytes gives the same bits as a fresh one, and so does a second call on it
-    (the counters are cleared per call; the groups are summed in a fixed
-    order)."""
+def test_route_split_k_on_a_dirty_workspace(w, cuda_lib):
+    """Few tokens: the router's split-K partial tiles meet in the route
+    workspace. A workspace full of 0xFF bytes gives the same bits as a fresh
+    one, and so does a second call on it (every tile is written before it is
+    read, and the splits are summed in a fixed order)."""
     inp = get_inputs(w, with_experts=False)
     cfg = binding.config(w)
     assert binding.route_workspace_size(cfg) > 0
