@@ -624,19 +624,35 @@ __global__ void __launch_bounds__(kRouterFinishThreads) router_finish_kernel(con
     }
     key[j] = kf;
   }
-  uint32_t taken = 0;   // bit j: entry j picked already
-  float sel_sum = 0.f, key0 = 0.f;
-  for (int r = 0; r < p.k; ++r) {
-    float kb = -INFINITY;
-    int ib = 0x7fffffff;   // no untaken entry: loses to any real one
+  // The lane's 8 (key, index) entries sorted once, larger key first and on
+  // equal keys the lower index (entries past E: -inf with an index above every
+  // real one). Each round then offers the lane's head entry to the group; the
+  // lane whose head wins drops it.
+  int idx[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = 8 * sub + j;
-      if (c < E && !((taken >> j) & 1u) && (key[j] > kb || ib == 0x7fffffff)) {
-        kb = key[j];
-        ib = c;
+  for (int j = 0; j < 8; ++j) idx[j] = 8 * sub + j < E ? 8 * sub + j : 0x7fffffff;
+  {
+    // an 8-input sorting network (19 comparators)
+    constexpr int net[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6}, {5, 7}, {1, 2},
+                                {5, 6}, {0, 4}, {3, 7}, {1, 5}, {2, 6}, {1, 4}, {3, 6}, {2, 4}, {3, 5},
+                                {3, 4}};
+#pragma unroll
+    for (int n = 0; n < 19; ++n) {
+      const int u = net[n][0], w = net[n][1];
+      if (better(key[w], idx[w], key[u], idx[u])) {
+        const float tk = key[u];
+        const int ti = idx[u];
+        key[u] = key[w];
+        idx[u] = idx[w];
+        key[w] = tk;
+        idx[w] = ti;
       }
     }
+  }
+  float sel_sum = 0.f, key0 = 0.f;
+  for (int r = 0; r < p.k; ++r) {
+    float kb = key[0];
+    int ib = idx[0];
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) {
       const float ko = __shfl_xor_sync(0xffffffffu, kb, o);
@@ -646,10 +662,18 @@ __global__ void __launch_bounds__(kRouterFinishThreads) router_finish_kernel(con
         ib = io;
       }
     }
-    // k <= E leaves an untaken entry every round; the clamp only keeps the
-    // row access in bounds regardless
+    if (ib == idx[0]) {   // this lane's head was picked: drop it
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        key[j] = key[j + 1];
+        idx[j] = idx[j + 1];
+      }
+      key[7] = -INFINITY;
+      idx[7] = 0x7fffffff;
+    }
+    // k <= E leaves a real entry every round; the clamp only keeps the row
+    // access in bounds regardless
     const int bi = min(max(ib, 0), EPAD - 1);
-    if (bi / 8 == sub) taken |= 1u << (bi % 8);
     float v;
     if (p.noisy) {
       if (r == 0) key0 = kb;
