@@ -335,6 +335,23 @@ moe_status device_state(DeviceState** out) {
     MOE_ROUTER_ATTR(__nv_bfloat16, 64) MOE_ROUTER_ATTR(__nv_bfloat16, 128)
     MOE_ROUTER_ATTR(__nv_bfloat16, 256)
 #undef MOE_ROUTER_ATTR
+    // The forward's small kernels prefer the largest shared-memory carveout, so
+    // that an SM running them can already take a CTA of the next, large-smem
+    // kernel (a programmatic dependent) instead of draining to reconfigure.
+    const int carve = cudaSharedmemCarveoutMaxShared;
+    ok &= cudaFuncSetAttribute(router_split_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carve) ==
+          cudaSuccess;
+    ok &= cudaFuncSetAttribute(count_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carve) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(scan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carve) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(scatter_kernel<__nv_bfloat16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               carve) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(combine_rows_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carve) ==
+          cudaSuccess;
+#define MOE_FINISH_CARVE(EP)                                                                     \
+  ok &= cudaFuncSetAttribute(router_finish_kernel<EP>, cudaFuncAttributePreferredSharedMemoryCarveout, \
+                             carve) == cudaSuccess;
+    MOE_FINISH_CARVE(32) MOE_FINISH_CARVE(64) MOE_FINISH_CARVE(128) MOE_FINISH_CARVE(256)
+#undef MOE_FINISH_CARVE
     if (!ok) return MOE_ERR_CUDA;
     s.ready = true;
   }

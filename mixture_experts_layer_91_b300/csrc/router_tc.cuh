@@ -11,12 +11,12 @@
 //     each difference exact in fp32, so the planes carry all 24 significand
 //     bits of W (8 each);
 //   * each product x_k * plane_k is exact in fp32 (8 x 8 significand bits);
-//   * the tensor core sums only short runs: every kRtcChunk k-blocks (128
+//   * the tensor core sums only short runs: every kRtcChunk k-blocks (256
 //     k-elements) the partial sums are drained from tensor memory and added
 //     into fp32 registers with ordinary round-to-nearest adds. The tensor
 //     core's own accumulation is not an IEEE add chain: over a whole row of
 //     d = 4096 its rounding reached ~1e-5 on logits of size ~4, the size of
-//     the routing margin; over 128 elements it stays far below.
+//     the routing margin; over 256 elements it stays far below.
 // So the logits are an fp32 dot product of the exact inputs, as the fp32
 // router asks ("Mixture of Experts" notes, section 5, ST-MoE precision).
 //
@@ -27,10 +27,11 @@
 //               which the split kernel just before writes (programmatic
 //               dependent launch);
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               M=128 K=16: one N = 2 NP MMA over the stacked hi | mid planes
-//               and one N = NP MMA adding lo onto mid (lo's products are 2^-9
-//               of mid's, so sharing their accumulator costs nothing), into
-//               2-4 accumulator buffers rotated over chunks;
+//               M=128 K=16: for NP <= 64 one N = 3 NP MMA over the three
+//               stacked planes; for NP = 128 one N = 256 MMA over hi | mid and
+//               one N = 128 MMA adding lo onto mid (lo's products are 2^-9 of
+//               mid's, so sharing their accumulator costs nothing); into 2-4
+//               accumulator buffers rotated over chunks;
 //   warps 2-9   drain each chunk: warp w reads the TMEM lanes of quarter
 //               w % 4 (one token per thread) and one half of the NP columns
 //               (warps 2-5 the first, 6-9 the second; at NP = 32 warps 2-5 all
@@ -48,7 +49,7 @@
 namespace moe {
 
 constexpr int kRtcThreads = 320;
-constexpr int kRtcChunk = 2;   // k-blocks (of 64) per tensor-memory drain
+constexpr int kRtcChunk = 4;   // k-blocks (of 64) per tensor-memory drain
 
 template <int NP>
 struct RtcShape {
@@ -62,11 +63,16 @@ struct RtcShape {
   static constexpr int WS = NP == 128 ? 2 : 3;
   static constexpr int XS = NP == 32 ? 11 : (NP == 64 ? 9 : 8);
   static constexpr uint32_t RING_BYTES = XS * A_BYTES + WS * W_BYTES;
-  // One accumulator buffer holds hi | (mid + lo) side by side (2 NP columns).
-  // Up to four buffers let the MMAs run three chunks ahead of the drains.
-  static constexpr uint32_t BUF_COLS = 2 * NP;
-  static constexpr int NBUF = 512 / BUF_COLS < 4 ? 512 / BUF_COLS : 4;
-  static constexpr uint32_t TMEM_COLS = NBUF * BUF_COLS;   // 256 or 512: a power of two
+  // One accumulator buffer holds the planes' partial sums side by side: for
+  // NP <= 64 hi | mid | lo (3 NP columns, one N = 3 NP MMA per K step over the
+  // three stacked planes); for NP = 128 hi | (mid + lo) (one N = 256 MMA over
+  // hi | mid and one N = 128 MMA adding lo onto the mid columns). Buffers sit at
+  // power-of-two column strides; up to four let the MMAs run ahead of the drains.
+  static constexpr bool ONE_MMA = NP <= 64;
+  static constexpr uint32_t BUF_COLS = ONE_MMA ? 3 * NP : 2 * NP;
+  static constexpr uint32_t BUF_STRIDE = BUF_COLS <= 128 ? 128 : 256;
+  static constexpr int NBUF = 512 / BUF_STRIDE < 4 ? 512 / BUF_STRIDE : 4;
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t BAR_BYTES = 512;
   static constexpr size_t smem_bytes = 1024 + static_cast<size_t>(RING_BYTES) + BAR_BYTES;
   static_assert(16 * (XS + WS) + 16 * NBUF + 16 <= BAR_BYTES, "barrier area");
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
         const uint32_t b = ch % S::NBUF;
         if (!mbar_wait(bar_tempty + 8 * b, ((ch / S::NBUF) & 1u) ^ 1u, abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t acc = tmem_base + b * S::BUF_COLS;
+        const uint32_t acc = tmem_base + b * S::BUF_STRIDE;
         for (int32_t j = 0; j < kRtcChunk && kb < nk; ++j, ++kb) {
           const uint32_t sx = kb % S::XS, sw = kb % S::WS;
           if (!mbar_wait(x_full + 8 * sx, (kb / S::XS) & 1u, abort) ||
@@ -242,12 +248,18 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
           const uint64_t ad = sdesc_kmajor_sw128(sX + sx * S::A_BYTES);
           const uint64_t bd = sdesc_kmajor_sw128(sW + sw * S::W_BYTES);   // hi, mid rows stacked
           const uint64_t bl = sdesc_kmajor_sw128(sW + sw * S::W_BYTES + 2 * S::B_BYTES);
-          constexpr uint32_t idesc2 = idesc_bf16_f32(128, 2 * NP);
-          constexpr uint32_t idesc1 = idesc_bf16_f32(128, NP);
+          if constexpr (S::ONE_MMA) {
+            constexpr uint32_t idesc3 = idesc_bf16_f32(128, 3 * NP);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc2, (j | kk) != 0);
-            tc_mma_bf16(acc + NP, ad + 2 * kk, bl + 2 * kk, idesc1, 1);
+            for (int kk = 0; kk < 4; ++kk) tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc3, (j | kk) != 0);
+          } else {
+            constexpr uint32_t idesc2 = idesc_bf16_f32(128, 2 * NP);
+            constexpr uint32_t idesc1 = idesc_bf16_f32(128, NP);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              tc_mma_bf16(acc, ad + 2 * kk, bd + 2 * kk, idesc2, (j | kk) != 0);
+              tc_mma_bf16(acc + NP, ad + 2 * kk, bl + 2 * kk, idesc1, 1);
+            }
           }
           tc_commit(x_empty + 8 * sx);
           tc_commit(w_empty + 8 * sw);
@@ -286,13 +298,22 @@ __global__ void __launch_bounds__(kRtcThreads, 1)
     if (drains) {
 #pragma unroll
       for (int cc = 0; cc < NH / 32; ++cc) {
-        const uint32_t col = tl + b * S::BUF_COLS + cc * 32;
+        const uint32_t col = tl + b * S::BUF_STRIDE + cc * 32;
         uint32_t hi[32], ml[32];
         tmem_ld_32x32b_x32(col, hi);
         tmem_ld_32x32b_x32(col + NP, ml);
-        tmem_ld_wait();
+        if constexpr (S::ONE_MMA) {   // mid and lo in their own columns: mid + lo first
+          uint32_t lo[32];
+          tmem_ld_32x32b_x32(col + 2 * NP, lo);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(ml[j]);
+          for (int j = 0; j < 32; ++j)
+            acc[cc * 32 + j] += __uint_as_float(hi[j]) + (__uint_as_float(ml[j]) + __uint_as_float(lo[j]));
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(hi[j]) + __uint_as_float(ml[j]);
+        }
       }
     }
     tc_fence_before();
