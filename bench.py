@@ -447,6 +447,49 @@ def run_reference(args, w):
     return 0
 
 
+def run_route_only(args, w) -> int:
+    """The router stage alone: `steps` back-to-back moe_route calls captured in
+    a CUDA graph (so the host's launch cost stays out) and replayed `warmup`
+    times untimed, then 10 times between CUDA events. x is larger than L2 at
+    the prefill sizes; the router's weight planes stay in L2 between calls."""
+    from mixture_experts_layer_91_b300 import binding
+    torch.cuda.set_device(0)
+    inp = inputs.make_inputs(w, with_experts=False)
+    cfg = binding.config(w)
+    g = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    ws = torch.empty(max(binding.route_workspace_size(cfg), 16), dtype=torch.uint8, device="cuda")
+    call = (cfg, g["x"], g["W_g"], g["W_noise"], g["eps"], g["bias"])
+    for _ in range(args.warmup):
+        binding.route(*call, workspace=ws)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(args.steps):
+                binding.route(*call, workspace=ws)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    st, raw = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device fault flag {raw} after the router's timed region")
+    us = e0.elapsed_time(e1) * 1e3 / (reps * args.steps)
+    x_bytes = w.T * w.d * (4 if w.fp32 else 2)
+    print(json.dumps({"metric": "moe_route time per call", "value": us, "unit": "us", "workload": w.name,
+                      "calls": reps * args.steps, "x_bytes": x_bytes,
+                      "x_read_gbs": x_bytes / (us * 1e-6) / 1e9, "note": "CUDA-graph replay, back to back"}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,6 +501,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time moe_route alone (a CUDA graph of back-to-back calls) and print one JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workloads.BY_NAME[args.workload]
@@ -465,6 +510,8 @@ def main():
         w = w.with_tokens(args.tokens)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.route_only:
+        return run_route_only(args, w)
 
     from mixture_experts_layer_91_b300 import binding
 
