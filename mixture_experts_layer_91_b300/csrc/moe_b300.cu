@@ -666,9 +666,14 @@ moe_status launch_experts(const moe_config* c, const DeviceState* ds, const void
     a.n_out = I;
     a.zero_out = reinterpret_cast<float4*>(zero);
     a.zero_n4 = zero != nullptr ? zero_n4 : 0;
-    if (!down_only)
-      MOE_TRY(launch_dependent(grouped_gemm_tc<kEpiSwiGLU>, dim3(grid), dim3(kTcThreads),
-                               tc_smem_bytes(kEpiSwiGLU), st, gu, a));
+    // An ordinary launch, not a programmatic dependent of the scatter: its CTAs
+    // resident early (one per SM, 200 KB of shared memory) took the scatter's
+    // later waves' room and cost the 16B-shaped layer 4 % (1.834 -> 1.753 ms,
+    // the 2B-shaped layer 0.460 -> 0.457 ms).
+    if (!down_only) {
+      grouped_gemm_tc<kEpiSwiGLU><<<grid, kTcThreads, tc_smem_bytes(kEpiSwiGLU), st>>>(gu, a);
+      MOE_TRY(last_launch());
+    }
     if (mark) MOE_TRY((*mark)(3));
 
     a.K = I;
