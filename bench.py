@@ -297,6 +297,37 @@ def backward_flops(w, kept: int) -> dict:
             "wgrad": w.n_mats * unit, "algorithmic": 2 * w.n_mats * unit + 2 * router}
 
 
+def route_launches(w, sm_count: int) -> int:
+    """Kernels one moe_route launches, by the library's choice of router:
+    split + tensor-core router + finish (bf16, <= 128 router columns,
+    T >= 4096); split-K partial + finish (T <= 512 with at least two splits of
+    the 64-deep chunks, at most 32, about one CTA per SM); else one CTA or
+    cluster per 32 tokens."""
+    cols = (2 if w.noisy else 1) * w.n_routed
+    if not w.fp32 and cols <= 128 and w.T >= 4096:
+        return 3
+    if w.T <= 512:
+        nblk = (w.T + 31) // 32
+        nsplit = min((w.d + 63) // 64, 32, sm_count // nblk)
+        if nsplit >= 2:
+            return 2
+    return 1
+
+
+def forward_launches(w, sm_count: int) -> int:
+    """Kernels of one forward: the route, count + scan + scatter, the two
+    expert GEMMs, and for bf16 layers the combine (rows) or the cast (scatter-add)."""
+    return route_launches(w, sm_count) + 3 + 2 + (0 if w.fp32 else 1)
+
+
+def backward_launches(w, sm_count: int) -> int:
+    """Kernels of one moe_backward of a bf16 layer: the route, count + scan +
+    scatter, the dy gather, a/b/g h, dh, the router softmax backward, dX, the
+    router's gradient terms on the tensor cores (weight planes, plans, dx term,
+    dW term, its reduction), the per-token dx sum and the weight gradients."""
+    return route_launches(w, sm_count) + 15
+
+
 def backward_line(args, w, layer, inp, x, eps, stream, barrier, kept: int, pk: dict, pk_kind: str) -> dict:
     """Time moe_backward (stage events inside the call, on its stream) over
     the same inputs and a seeded upstream gradient: the layer's backward with
@@ -356,10 +387,7 @@ def backward_line(args, w, layer, inp, x, eps, stream, barrier, kept: int, pk: d
              "tflops": (fwd_flops + fl["algorithmic"]) / ((f_ms + b_ms) / 1e3) / 1e12,
              "note": "moe_forward_train + moe_backward_from_forward: the backward reuses the forward's routing, "
                      "dispatch and saved a, b, g h"}
-    # [W split] + router + count + scan + scatter + gather + save + dh + router bwd + dx
-    # + router dW + router dx + dx sum + wgrad (dW_g cleared by a memset)
-    tc_router = (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
-    launches = 14 + (1 if tc_router else 0)
+    launches = backward_launches(w, torch.cuda.get_device_properties(dev).multi_processor_count)
     top = max(("save", "dh", "dx", "wgrad"), key=lambda n: stage_ms[n])
     achieved = gemm[top]
     return {"ms_per_step": ms, "tokens_per_s": w.T / (ms / 1e3),
@@ -609,10 +637,7 @@ def main():
     tflops = world * flops / (ms_step / 1e3) / 1e12
     ab = algorithmic_bytes(w, touched)
     roof_time = max(flops / (pk["bf16_tflops"] * 1e12), ab / (pk["hbm_gbs"] * 1e9))
-    # bf16: [W split] + router + count + scan + rank + gate-up + down + (combine | cast);
-    # fp32: router + count + scan + scatter + gate-up + down
-    tc_router = (not w.fp32) and (2 if w.noisy else 1) * w.n_routed <= 128 and w.T >= 4096
-    launches_per_step = 6 if w.fp32 else (8 if tc_router else 7)
+    launches_per_step = forward_launches(w, torch.cuda.get_device_properties(dev).multi_processor_count)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

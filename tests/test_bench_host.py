@@ -105,3 +105,22 @@ def test_backward_flops_count_each_weight_product_twice():
         assert fl["save"] == pytest.approx(fwd["gate_up"])
         assert fl["dh"] + fl["dx"] + fl["wgrad"] == pytest.approx(2 * (fwd["gate_up"] + fwd["down"]))
         assert fl["algorithmic"] == pytest.approx(2 * (fwd["gate_up"] + fwd["down"]) + 2 * fwd["router"])
+
+
+def test_launch_counts_follow_the_router_choice():
+    """Kernels per forward / backward, as the launch lists of a B300 (148 SMs)
+    show them: the 16B layer routes through split + tensor-core router + finish
+    (9 forward kernels, 18 backward), the 145B decode (T = 64) through split-K
+    partial + finish (8), the tiny fp32 layer through split-K too but with no
+    combine kernel (7), and a 1000-token bf16 layer through one cluster router (7)."""
+    import bench
+    from mixture_experts_layer_91_b300 import workloads as W
+    assert bench.forward_launches(W.DSMOE_16B, 148) == 9
+    assert bench.backward_launches(W.DSMOE_16B, 148) == 18
+    assert bench.forward_launches(W.DSMOE_2B, 148) == 9
+    assert bench.forward_launches(W.DSMOE_145B_DECODE, 148) == 8
+    assert bench.forward_launches(W.TINY_FP32, 148) == 7
+    assert bench.forward_launches(W.DSMOE_16B.with_tokens(1000), 148) == 7
+    # noisy with 2 x 64 router columns still fits the tensor-core router
+    assert bench.route_launches(W.replace(W.GSHARD_NOISY, n_routed=64), 148) == 3
+    assert bench.route_launches(W.replace(W.GSHARD_NOISY, n_routed=65), 148) == 1
