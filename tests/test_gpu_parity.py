@@ -160,6 +160,30 @@ def test_route_tensor_core_odd_shapes(w, cuda_lib):
     test_route(w, cuda_lib)
 
 
+# The router's three forms at their boundaries: split-K partial + finish for
+# T <= 512, one CTA or cluster per 32 tokens above, the tensor-core router for
+# bf16 at T >= 4096 (<= 128 router columns); 256 router columns (EPAD 256) on the
+# CUDA-core forms; an fp32 layer with many splits of a long d; noisy at T = 64.
+ROUTE_EDGES = [
+    workloads.Workload("route_T512_bf16", T=512, d=1024, n_routed=64, n_shared=0, top_k=6, d_ff=64, seed=61),
+    workloads.Workload("route_T513_bf16", T=513, d=1024, n_routed=64, n_shared=0, top_k=6, d_ff=64, seed=62),
+    workloads.Workload("route_T4095_bf16", T=4095, d=512, n_routed=64, n_shared=0, top_k=6, d_ff=64, seed=63),
+    workloads.Workload("route_T4096_bf16", T=4096, d=512, n_routed=64, n_shared=0, top_k=6, d_ff=64, seed=64),
+    workloads.Workload("route_T64_E256_bf16", T=64, d=2048, n_routed=256, n_shared=0, top_k=8, d_ff=64,
+                       bias=True, seed=65),
+    workloads.Workload("route_T700_E256_bf16", T=700, d=512, n_routed=256, n_shared=0, top_k=8, d_ff=64, seed=66),
+    workloads.Workload("route_T300_d4096_fp32", T=300, d=4096, n_routed=40, n_shared=0, top_k=4, d_ff=64,
+                       fp32=True, seed=67),
+    workloads.Workload("route_T64_noisy_bf16", T=64, d=1024, n_routed=32, n_shared=0, top_k=2, d_ff=64,
+                       renormalize=True, noisy=True, seed=68),
+]
+
+
+@pytest.mark.parametrize("w", ROUTE_EDGES, ids=lambda w: w.name)
+def test_route_forms_at_their_boundaries(w, cuda_lib):
+    test_route(w, cuda_lib)
+
+
 @pytest.mark.parametrize("w", [workloads.DSMOE_145B_DECODE, RAGGED], ids=lambda w: w.name)
 def test_route_split_k_on_a_dirty_workspace(w, cuda_lib):
     """Few tokens: the router's split-K partial tiles meet in the route
