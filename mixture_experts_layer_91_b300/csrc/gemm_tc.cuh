@@ -317,6 +317,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool valid = false;
       int64_t orow = 0;
       float gate = 1.0f;
+      // bf16 rows: a warp whose 32 rows all lie past the group's rows (tile
+      // padding, read by nothing) stores nothing
+      const bool rows_here = MODE != kEpiStoreBf16 || c.lmt * kTcBM + q * 32 < __ldg(p.plan.gsize + c.g);
       if (MODE == kEpiScatterAdd || MODE == kEpiStoreRows) {
         valid = row_local < __ldg(p.plan.gsize + c.g);
         if (valid) {
@@ -383,14 +386,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       } else if (MODE == kEpiStoreBf16) {
         // The tile's 128 x 256 fp32 accumulator as bf16 rows at its padded H
-        // rows (padding rows included: they fall inside the tile's own group),
-        // in 32 x 32 boxes through the same double-buffered 64-byte-swizzled
-        // staging as the gate-up's H stores. Boxes starting past the last
-        // column are skipped; TMA clips a box that straddles it.
+        // rows, in 32 x 32 boxes through the same double-buffered
+        // 64-byte-swizzled staging as the gate-up's H stores. A warp's boxes are
+        // skipped when its 32 rows are all tile padding (nothing reads them: the
+        // combine addresses the group's own rows only), and so are boxes starting
+        // past the last column; TMA clips a box that straddles it.
         const uint32_t buf0 = sStore + ew * 2 * kStoreBoxBytes;
         const int32_t col0 = c.nt * kTcBN;
 #pragma unroll 1
-        for (int cc = 0; cc < kTcBN / 32 && col0 + cc * 32 < p.n_out; ++cc, ++nstore) {
+        for (int cc = 0; rows_here && cc < kTcBN / 32 && col0 + cc * 32 < p.n_out; ++cc, ++nstore) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + cc * 32, v);
           tmem_ld_wait();
