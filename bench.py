@@ -300,18 +300,12 @@ def backward_flops(w, kept: int) -> dict:
 def route_launches(w, sm_count: int) -> int:
     """Kernels one moe_route launches, by the library's choice of router:
     split + tensor-core router + finish (bf16, <= 128 router columns,
-    T >= 4096); split-K partial + finish (T <= 512 with at least two splits of
-    the 64-deep chunks, at most 32, about one CTA per SM); else one CTA or
-    cluster per 32 tokens."""
+    T >= 4096); otherwise a CUDA-core router (split-K partial tiles for T <= 512
+    with at least two splits, else one CTA or cluster per 32 tokens) + finish."""
     cols = (2 if w.noisy else 1) * w.n_routed
     if not w.fp32 and cols <= 128 and w.T >= 4096:
         return 3
-    if w.T <= 512:
-        nblk = (w.T + 31) // 32
-        nsplit = min((w.d + 63) // 64, 32, sm_count // nblk)
-        if nsplit >= 2:
-            return 2
-    return 1
+    return 2
 
 
 def forward_launches(w, sm_count: int) -> int:

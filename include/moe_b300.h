@@ -134,11 +134,13 @@ const char* moe_status_string(int status);
 /* Library ABI version: (major << 16) | minor. */
 int moe_version(void);
 
-/* Bytes of scratch moe_route needs. Tensor-core router: the three bf16
- * planes of the router weights. CUDA-core router (fp32 tokens, more than 128
- * router columns, or T < 4096) with T <= 512: the partial logits tiles of the
- * split of the reduction over d among more SMs (written before they are read:
- * the scratch needs no initialisation). Otherwise 0. */
+/* Bytes of scratch moe_route needs (0 only for T = 0): the router's fp32
+ * logits rows, which a second kernel turns into softmax, keys, top-k and
+ * gates. Tensor-core router (bf16 tokens, <= 128 router columns, T >= 4096):
+ * the three bf16 planes of the router weights, then one logits row per token.
+ * CUDA-core router: for T <= 512 the partial logits tiles of the split of the
+ * reduction over d among more SMs, else one logits row per token. Everything
+ * is written before it is read: the scratch needs no initialisation. */
 size_t moe_route_workspace_size(const moe_config* cfg);
 
 /*

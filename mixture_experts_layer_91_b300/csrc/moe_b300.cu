@@ -96,10 +96,13 @@ int router_epad(const moe_config* c) {
   return cols <= 32 ? 32 : (cols <= 64 ? 64 : (cols <= 128 ? 128 : 256));
 }
 
-// Bytes of the split-K partial logits tiles ([block][split][32][EPAD] fp32);
-// 0 where the split-K form does not run.
+// Bytes of the CUDA-core router's logits rows for router_finish_kernel: the
+// split-K partial tiles ([block][split][32][EPAD] fp32) for T <= 512, else one
+// row per token ([T][EPAD], the one split of the same layout); 0 for the
+// tensor-core router (its scratch is router_scratch_bytes') or T = 0.
 size_t router_group_bytes(const moe_config* c) {
-  if (router_tc_np(c) > 0 || c->T == 0 || c->T > kRouterSplitMaxTokens) return 0;
+  if (router_tc_np(c) > 0 || c->T == 0) return 0;
+  if (c->T > kRouterSplitMaxTokens) return static_cast<size_t>(c->T) * router_epad(c) * 4;
   const int64_t nblk = (c->T + kRouterBT - 1) / kRouterBT;
   return static_cast<size_t>(nblk) * kRouterMaxSplits * kRouterBT * router_epad(c) * 4;
 }
@@ -532,8 +535,8 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
   // Few tokens (T <= 512): split-K over independent CTAs, about one per SM,
   // then the finish kernel (a programmatic dependent) per 8 tokens.
   const int64_t nsplit = std::min<int64_t>(std::min<int64_t>(nchunk, kRouterMaxSplits), sm_count / nblk);
-  if (router_group_bytes(c) > 0 && nsplit >= 2) {
-    a.part = static_cast<float*>(scratch);
+  a.part = static_cast<float*>(scratch);
+  if (c->T <= kRouterSplitMaxTokens && nsplit >= 2) {
     const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>(nsplit));
     // the finish kernel: enough tokens per CTA for an element per thread, or
     // about one CTA per SM if that takes more (at most 256 / (EPAD / 8))
@@ -583,7 +586,17 @@ moe_status launch_route(const moe_config* c, const void* x, const float* W_g, co
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
-  return last_launch();
+  MOE_TRY(last_launch());
+  // softmax, keys, top-k and gates: the finish kernel over the logits rows as
+  // the one split of its layout (EPAD / 8 lanes per token)
+  const int32_t ep = router_epad(c);
+  const int32_t tpc = kRouterFinishThreads * 8 / ep;
+  const dim3 fgrid(static_cast<unsigned>((c->T + tpc - 1) / tpc));
+  const dim3 fblock(kRouterFinishThreads);
+  if (ep == 32) return launch_dependent(router_finish_kernel<32>, fgrid, fblock, 0, st, a, 1, tpc);
+  if (ep == 64) return launch_dependent(router_finish_kernel<64>, fgrid, fblock, 0, st, a, 1, tpc);
+  if (ep == 128) return launch_dependent(router_finish_kernel<128>, fgrid, fblock, 0, st, a, 1, tpc);
+  return launch_dependent(router_finish_kernel<256>, fgrid, fblock, 0, st, a, 1, tpc);
 }
 
 moe_status launch_permute(const moe_config* c, const DeviceState* ds, const void* x,

@@ -20,10 +20,11 @@
 // memory in a fixed order. When T is small a thread-block cluster of CS CTAs
 // also splits the k-chunks; each CTA of the cluster then owns BT / CS of the
 // tokens and adds their partial rows from every CTA's tile through
-// distributed shared memory (ranks in order). With very few tokens (T <= 512)
-// a grid of independent CTAs splits the chunks instead, and a second kernel
-// sums each token's partial rows in split order. Per token, one warp computes
-// the softmax and a k-round warp arg-max (ties to the lower index).
+// distributed shared memory (ranks in order) and stores their logits rows.
+// With very few tokens (T <= 512) a grid of independent CTAs splits the chunks
+// instead and stores partial rows. Either way router_finish_kernel then adds
+// each token's rows in split order and computes its softmax, keys and k
+// arg-max rounds (ties to the lower index).
 #pragma once
 
 #include "common.cuh"
@@ -332,98 +333,6 @@ __device__ __forceinline__ void router_block_logits(const RouterArgs& p, float* 
   __syncthreads();
 }
 
-// Softmax, keys, top-k and gates of token t from its logits row Lr (EPAD
-// columns: the N_r gate logits, then the noise logits when noisy); one warp.
-// The per-expert statistic sums go to the CTA's s_prob / s_gate.
-template <int EPAD>
-__device__ __forceinline__ void router_token(const RouterArgs& p, const float* Lr, int64_t t, int lane,
-                                             float* s_prob, float* s_gate) {
-  constexpr int PER_LANE = EPAD / 32;
-  float lg[PER_LANE], key[PER_LANE], sv[PER_LANE];
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) {
-    const int cc = lane + 32 * i;
-    lg[i] = (cc < p.E) ? Lr[cc] : -INFINITY;
-    m = fmaxf(m, lg[i]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float ssum = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) {
-    const int cc = lane + 32 * i;
-    sv[i] = (cc < p.E) ? expf(lg[i] - m) : 0.f;
-    ssum += sv[i];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-  const float inv = 1.0f / ssum;
-  if (p.lse != nullptr && lane == 0) p.lse[t] = m + logf(ssum);
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) {
-    const int cc = lane + 32 * i;
-    sv[i] *= inv;
-    if (p.prob_sum != nullptr && cc < p.E) atomicAdd(&s_prob[cc], sv[i]);
-    if (cc >= p.E) {
-      key[i] = -INFINITY;
-    } else if (p.noisy) {
-      key[i] = lg[i] + p.eps[t * p.E + cc] * softplus_f(Lr[p.E + cc]);
-    } else if (p.bias != nullptr) {
-      key[i] = sv[i] + p.bias[cc];
-    } else {
-      key[i] = lg[i];   // Softmax is increasing: the order of s is the order of the logits
-    }
-    if (key[i] != key[i]) key[i] = -INFINITY;   // a NaN key ranks last, ids stay valid
-    if (p.logits_out != nullptr && cc < p.E) p.logits_out[t * p.E + cc] = lg[i];
-    if (p.noise_out != nullptr && cc < p.E) p.noise_out[t * p.E + cc] = Lr[p.E + cc];
-  }
-
-  uint32_t taken = 0;
-  int my_id = 0;
-  float my_val = 0.f;   // s of the pick (softmax gate) or its key H (noisy)
-  float sel_sum = 0.f, key0 = 0.f;
-  for (int r = 0; r < p.k; ++r) {
-    float kb = -INFINITY, vb = 0.f;
-    int ib = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int cc = lane + 32 * i;
-      if (cc < p.E && !((taken >> i) & 1u) && better(key[i], cc, kb, ib)) {
-        kb = key[i];
-        ib = cc;
-        vb = p.noisy ? key[i] : sv[i];
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ko = __shfl_xor_sync(0xffffffffu, kb, o);
-      const int io = __shfl_xor_sync(0xffffffffu, ib, o);
-      const float vo = __shfl_xor_sync(0xffffffffu, vb, o);
-      if (better(ko, io, kb, ib)) {
-        kb = ko;
-        ib = io;
-        vb = vo;
-      }
-    }
-    if ((ib & 31) == lane) taken |= 1u << (ib >> 5);
-    if (r == 0) key0 = vb;
-    if (p.noisy) vb = expf(vb - key0);   // softmax over the kept H (max is the first pick)
-    sel_sum += vb;
-    if (lane == r) {
-      my_id = ib;
-      my_val = vb;
-    }
-  }
-  if (lane < p.k) {
-    float g = my_val;
-    if (p.noisy || p.renorm) g = my_val / sel_sum;
-    p.topk_ids[t * p.k + lane] = my_id;
-    p.topk_w[t * p.k + lane] = g;
-    if (p.gate_sum != nullptr) atomicAdd(&s_gate[my_id], g);
-  }
-}
-
 // The CTA's statistic sums into the per-expert totals (after a __syncthreads).
 template <int EPAD>
 __device__ __forceinline__ void router_flush_stats(const RouterArgs& p, const float* s_prob, const float* s_gate) {
@@ -445,28 +354,20 @@ __device__ __forceinline__ void router_zero_rows(const RouterArgs& p, int64_t t_
 }
 
 // One CTA per BT tokens; a cluster of CS CTAs (CS >= 1) splits the chunks and
-// each CTA finishes BT / CS of the tokens.
+// each CTA stores BT / CS of the tokens' logits rows to part[T][EPAD] (the one
+// split of router_finish_kernel's layout), which then finishes the tokens.
 template <typename TX, int EPAD>
 __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_kernel(const RouterArgs p) {
   using S = RouterShape<EPAD>;
   extern __shared__ __align__(16) float rsm[];
-  pdl_launch_dependents();   // the dispatch kernels may launch and wait for this one
+  pdl_launch_dependents();   // the finish kernel may launch and wait for this one
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_rank();
   const uint32_t csize = cluster_size();
   const int64_t t0 = static_cast<int64_t>(blockIdx.x / csize) * S::BT;
-  __shared__ float s_prob[EPAD], s_gate[EPAD];   // per-CTA statistic sums
-  for (int c = tid; c < EPAD; c += kRouterThreads) {
-    s_prob[c] = 0.f;
-    s_gate[c] = 0.f;
-  }
-  // the clear of the tokens' fp32 accumulator rows is shared among the cluster
-  router_zero_rows(p, t0, (p.T - t0 < S::BT) ? p.T : t0 + S::BT, tid + static_cast<int64_t>(crank) * kRouterThreads,
-                   static_cast<int64_t>(kRouterThreads) * csize);
   router_block_logits<TX, EPAD>(p, rsm, t0, static_cast<int>(crank), static_cast<int>(csize));
   float* part = rsm;
-  // Tokens this CTA finishes: all of the tile, or with a cluster its rank's
+  // Tokens this CTA stores: all of the tile, or with a cluster its rank's
   // share (BT / csize consecutive tokens).
   int tok_begin = 0, tok_end = S::BT;
   if (csize > 1) {
@@ -493,14 +394,14 @@ __global__ void __launch_bounds__(kRouterThreads, EPAD <= 64 ? 2 : 1) router_ker
     }
     cluster_sync_all();   // no CTA leaves while another still reads its tile
   }
-  // per-token softmax + top-k: one warp per token
-  for (int tok = tok_begin + warp; tok < tok_end; tok += kRouterWarps) {
+  // the rows of this CTA's tokens, 16 bytes at a time
+  for (int idx = tid; idx < (tok_end - tok_begin) * (EPAD / 4); idx += kRouterThreads) {
+    const int tok = tok_begin + idx / (EPAD / 4), col = 4 * (idx % (EPAD / 4));
     const int64_t t = t0 + tok;
-    if (t >= p.T) break;
-    router_token<EPAD>(p, part + tok * S::LS, t, lane, s_prob, s_gate);
+    if (t >= p.T) continue;
+    const float* r = part + tok * S::LS + col;
+    reinterpret_cast<float4*>(p.part + t * EPAD + col)[0] = make_float4(r[0], r[1], r[2], r[3]);
   }
-  __syncthreads();
-  router_flush_stats<EPAD>(p, s_prob, s_gate);
 }
 
 // Few tokens (T <= 512): split-K over a grid (token blocks, S) of independent

@@ -112,7 +112,8 @@ def test_launch_counts_follow_the_router_choice():
     show them: the 16B layer routes through split + tensor-core router + finish
     (9 forward kernels, 18 backward), the 145B decode (T = 64) through split-K
     partial + finish (8), the tiny fp32 layer through split-K too but with no
-    combine kernel (7), and a 1000-token bf16 layer through one cluster router (7)."""
+    combine kernel (7), and a 1000-token bf16 layer through the cluster router +
+    finish (8)."""
     import bench
     from mixture_experts_layer_91_b300 import workloads as W
     assert bench.forward_launches(W.DSMOE_16B, 148) == 9
@@ -120,7 +121,7 @@ def test_launch_counts_follow_the_router_choice():
     assert bench.forward_launches(W.DSMOE_2B, 148) == 9
     assert bench.forward_launches(W.DSMOE_145B_DECODE, 148) == 8
     assert bench.forward_launches(W.TINY_FP32, 148) == 7
-    assert bench.forward_launches(W.DSMOE_16B.with_tokens(1000), 148) == 7
+    assert bench.forward_launches(W.DSMOE_16B.with_tokens(1000), 148) == 8
     # noisy with 2 x 64 router columns still fits the tensor-core router
     assert bench.route_launches(W.replace(W.GSHARD_NOISY, n_routed=64), 148) == 3
-    assert bench.route_launches(W.replace(W.GSHARD_NOISY, n_routed=65), 148) == 1
+    assert bench.route_launches(W.replace(W.GSHARD_NOISY, n_routed=65), 148) == 2

@@ -123,8 +123,8 @@ def test_route_workspace_size_matches_the_router_choice(lib):
     rounded up to 32 / 64 / 128) and its fp32 logits rows (T x NP x 4 bytes),
     each region rounded up to 256 bytes. The CUDA-core router needs the split-K
     partial tiles for T <= 512 (token blocks of 32 x 32 splits x 32 tokens x
-    EPAD fp32, EPAD the columns rounded up to 32 / 64 / 128 / 256) and nothing
-    above."""
+    EPAD fp32, EPAD the columns rounded up to 32 / 64 / 128 / 256) and one fp32
+    logits row of EPAD columns per token above."""
     def up(b):
         return (b + 255) // 256 * 256
     big = dict(T=4096, d=256, act_dtype=1)
@@ -132,14 +132,16 @@ def test_route_workspace_size_matches_the_router_choice(lib):
                                         (16, 1, 1, 32), (64, 1, 1, 128)]:
         c = cfg_of(**big, n_routed=n_routed, gate=gate, renormalize=renorm)
         assert lib.moe_route_workspace_size(ctypes.byref(c)) == up(3 * np_ * 256 * 2) + up(4096 * np_ * 4)
-    for kw in (dict(T=4095), dict(act_dtype=0), dict(n_routed=129), dict(n_routed=65, gate=1, renormalize=1)):
+    # CUDA-core router above 512 tokens: one fp32 logits row of EPAD columns per token
+    for kw, T, epad in ((dict(T=4095), 4095, 64), (dict(act_dtype=0), 4096, 64), (dict(n_routed=129), 4096, 256),
+                        (dict(n_routed=65, gate=1, renormalize=1), 4096, 256)):
         c = cfg_of(**{**big, "n_routed": 64, **kw})
-        assert lib.moe_route_workspace_size(ctypes.byref(c)) == 0
+        assert lib.moe_route_workspace_size(ctypes.byref(c)) == T * epad * 4
     for T, n_routed, epad in [(64, 128, 128), (512, 64, 64), (33, 20, 32), (1, 200, 256)]:
         c = cfg_of(**{**big, "T": T, "n_routed": n_routed})
         assert lib.moe_route_workspace_size(ctypes.byref(c)) == (T + 31) // 32 * 32 * 32 * epad * 4
     c = cfg_of(**{**big, "T": 513, "n_routed": 64})
-    assert lib.moe_route_workspace_size(ctypes.byref(c)) == 0
+    assert lib.moe_route_workspace_size(ctypes.byref(c)) == 513 * 64 * 4
     # a workspace short of the planes is refused before any launch
     c = cfg_of(**big, n_routed=64)
     fake = ctypes.c_void_p(1 << 20)
