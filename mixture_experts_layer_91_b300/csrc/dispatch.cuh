@@ -87,15 +87,48 @@ struct PlanOut {
   int32_t* o_row;     // [G]
 };
 
+// Exclusive prefix sum of one value per thread over the whole block (thread
+// order), and the block's total. Every thread of the block calls it; integer
+// sums, so the result is the serial one exactly. warp_sums: shared, >= 32.
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_sums, int32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;   // inclusive over the warps
+  }
+  __syncthreads();
+  total = warp_sums[nw - 1];
+  const int32_t excl = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  __syncthreads();   // warp_sums free for the next call
+  return excl;
+}
+
 // Group plan from per-expert offsets (one CTA; called by scan_kernel and
 // plan_kernel). Groups: K_s shared (all T tokens, A rows from x), then N_r
 // routed (A rows from x_perm at offsets[e]). Unpadded per-row output: shared
 // group i at rows i*T, routed group e at K_s*T + offsets[e]. m-tiles are 128
 // rows; the padded H row of a group is 128 * mt_start[g].
 __device__ void plan_groups(const int32_t* offsets, int32_t E, int32_t K_s, int64_t T,
-                            const PlanOut& o, int32_t* s_tiles /* smem [G] */) {
+                            const PlanOut& o, int32_t* warp_sums /* smem [32] */) {
+  // one group per thread: G = K_s + E <= 64 + 256, below every caller's block size
   const int32_t G = K_s + E;
-  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+  const int g = threadIdx.x;
+  int32_t tiles = 0;
+  if (g < G) {
     int32_t size, arow;
     int64_t orow;
     if (g < K_s) {
@@ -111,17 +144,12 @@ __device__ void plan_groups(const int32_t* offsets, int32_t E, int32_t K_s, int6
     o.gsize[g] = size;
     o.a_row[g] = arow;
     o.o_row[g] = static_cast<int32_t>(orow);
-    s_tiles[g] = (size + kTcBM - 1) / kTcBM;
+    tiles = (size + kTcBM - 1) / kTcBM;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t run = 0;
-    for (int g = 0; g < G; ++g) {
-      o.mt_start[g] = run;
-      run += s_tiles[g];
-    }
-    o.mt_start[G] = run;
-  }
+  int32_t total;
+  const int32_t start = block_exclusive_scan(tiles, warp_sums, total);
+  if (g < G) o.mt_start[g] = start;
+  if (g == 0) o.mt_start[G] = total;
   __syncthreads();
 }
 
@@ -140,6 +168,7 @@ __global__ void __launch_bounds__(kScanThreads)
   pdl_launch_dependents();
   __shared__ int32_t tot[kMaxGroups + 1];
   __shared__ int32_t part[kScanThreads];
+  __shared__ int32_t s_wsum[32];   // block scans' warp totals
   // The histogram staged in shared memory when it fits (the headline-sized
   // layers): one round of independent coalesced loads, where the walks below
   // over global memory would wait a load latency per block.
@@ -175,15 +204,17 @@ __global__ void __launch_bounds__(kScanThreads)
     tot[threadIdx.x] = s;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t r = 0;
-    for (int i = 0; i < E; ++i) {
-      const int32_t c = capacity > 0 ? min(tot[i], capacity) : tot[i];
+  {
+    // accepted counts and their exclusive prefix (E <= 256: one expert per thread)
+    const int i = threadIdx.x;
+    const int32_t c = i < E ? (capacity > 0 ? min(tot[i], capacity) : tot[i]) : 0;
+    int32_t total;
+    const int32_t off = block_exclusive_scan(c, s_wsum, total);
+    if (i < E) {
       counts[i] = c;
-      offsets[i] = r;
-      r += c;
+      offsets[i] = off;
     }
-    offsets[E] = r;
+    if (i == 0) offsets[E] = total;
   }
   __syncthreads();
   if (active) {
@@ -198,16 +229,15 @@ __global__ void __launch_bounds__(kScanThreads)
   }
   if (with_plan) {
     __syncthreads();
-    __shared__ int32_t s_tiles[kMaxGroups];
-    plan_groups(offsets, E, K_s, T, plan, s_tiles);
+    plan_groups(offsets, E, K_s, T, plan, s_wsum);
   }
 }
 
 // Plan from caller-supplied offsets (the moe_expert_ffn stage entry point).
 __global__ void plan_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t K_s, int64_t T,
                             PlanOut plan) {
-  __shared__ int32_t s_tiles[kMaxGroups];
-  plan_groups(offsets, E, K_s, T, plan, s_tiles);
+  __shared__ int32_t s_wsum[32];
+  plan_groups(offsets, E, K_s, T, plan, s_wsum);
 }
 
 // dest / perm_src and the row gather. One warp per assignment, grid-stride.
