@@ -12,14 +12,18 @@ rank runs an independent replica on its own GPU (the layer's tokens are
 independent; no collective is on the data path): weak scaling.
 
 Prints one JSON line (rank 0). `value` is whole-job tokens/s (all ranks'
-tokens / max-over-ranks time); `e2e` is the same metric through the public
-API with the step's x copied in from pinned host memory and y copied back
-inside the timed region; `roofline` is the gate-up GEMM (the dominant kernel)
-measured live with CUDA events recorded inside the library call on the
-stream the kernels run on; `cpu_baseline` is the fp64 CPU oracle timed on a
+tokens / max-over-ranks time) over region 1, the plain forward back to back;
+`kernels_ms` and `roofline` (the gate-up GEMM, the dominant kernel) come from
+region 2, the same steps with CUDA events recorded between the stages inside
+the library call on the stream the kernels run on, after an idle second;
+`e2e` is the same metric through the public API with the step's x copied in
+from pinned host memory and y copied back inside the timed region;
+`backward` times moe_backward and a training step (moe_forward_train +
+moe_backward_from_forward); `cpu_baseline` is the fp64 CPU oracle timed on a
 bounded sample of the same workload.
 
 --impl reference times that oracle itself, as it stands, on the host cores.
+--route-only times moe_route alone (a CUDA graph of back-to-back calls).
 """
 
 from __future__ import annotations
