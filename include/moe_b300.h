@@ -381,14 +381,17 @@ moe_status moe_backward_profiled(const moe_config* cfg, const void* x, const flo
                                  void* const* stage_events);
 
 /*
- * moe_forward_train -- the forward of a training step: moe_forward's y, plus
- * the state the backward needs, left in `workspace` (>=
+ * moe_forward_train -- the forward of a training step: moe_forward's y (the
+ * layer of the DeepSeekMoE translation, section 3.2, eqs (9)-(11)), plus the
+ * state the backward needs, left in `workspace` (>=
  * moe_backward_workspace_size()): the routing, the logits (and noise logits),
  * the dispatch and group plan, x_perm, and the expert pre-activations a, b and
  * g * h. y is formed from g * h through W2 and the per-token sum of the rows
  * (the gates ride on g * h), so it is the sum of moe_forward; bf16 layers use
  * the row combine whatever cfg->combine says, fp32 layers the scatter-add.
- * Arguments as in moe_forward.
+ * Arguments as in moe_forward. Errors: MOE_ERR_INVALID_ARG for a missing or
+ * misaligned pointer, MOE_ERR_WORKSPACE for ws_bytes below
+ * moe_backward_workspace_size(); T = 0 does nothing.
  */
 moe_status moe_forward_train(const moe_config* cfg, const void* x, const float* W_g,
                              const float* W_noise, const float* eps, const float* bias,
@@ -396,8 +399,10 @@ moe_status moe_forward_train(const moe_config* cfg, const void* x, const float* 
                              void* workspace, size_t ws_bytes, void* y, void* stream);
 
 /*
- * moe_backward_from_forward -- moe_backward (same arguments, results and
- * precision) on a workspace that moe_forward_train filled for the same cfg,
+ * moe_backward_from_forward -- moe_backward (the gradients of the layer of the
+ * DeepSeekMoE translation, section 3.2, with the top-k selection held fixed;
+ * same arguments, results, precision and errors) on a workspace that
+ * moe_forward_train filled for the same cfg,
  * x, router weights, noise, bias and expert weights, with nothing in between
  * that wrote to it: the routing, the dispatch and the recompute of a, b and
  * g * h are skipped. It consumes the state (da and db overwrite the saved a
