@@ -183,3 +183,33 @@ def test_config_struct_matches_the_header():
     body = body[:body.index("} moe_config;")]
     names = re.findall(r"\b(?:int64_t|int32_t)\s+(\w+);", body)
     assert names == [f[0] for f in binding.MoeConfig._fields_]
+
+
+def test_backward_and_training_pair_refuse_bad_arguments_before_any_device_work(lib):
+    """moe_backward, moe_backward_from_forward and moe_forward_train check their
+    arguments on the host: missing or misaligned pointers give
+    MOE_ERR_INVALID_ARG and a workspace below moe_backward_workspace_size()
+    MOE_ERR_WORKSPACE, before anything is launched (the fake addresses are never
+    dereferenced). moe_forward_train with T = 0 does nothing."""
+    c = cfg_of(act_dtype=1, d=256, d_ff=128)
+    need = lib.moe_backward_workspace_size(ctypes.byref(c))
+    assert need > 0
+    f = ctypes.c_void_p(1 << 20)            # 16-byte aligned, never touched
+    odd = ctypes.c_void_p((1 << 20) + 2)    # misaligned
+    def bwd(fn, *, x=f, dy=f, ws_bytes=need, w1=f, dw1=f, dx=f, extra=()):
+        return fn(ctypes.byref(c), x, f, None, None, None, w1, f, f, dy, f, ws_bytes, dx, f, None, dw1, f, f,
+                  None, *extra)
+    for fn, extra in ((lib.moe_backward, ()), (lib.moe_backward_from_forward, (None,))):
+        assert bwd(fn, x=None, extra=extra) == 1
+        assert bwd(fn, dy=None, extra=extra) == 1
+        assert bwd(fn, w1=None, extra=extra) == 1
+        assert bwd(fn, dw1=None, extra=extra) == 1
+        assert bwd(fn, dx=odd, extra=extra) == 1
+        assert bwd(fn, ws_bytes=need - 1, extra=extra) == 3
+    def fwd_train(*, x=f, ws_bytes=need, y=f, T=None):
+        cc = c if T is None else cfg_of(act_dtype=1, d=256, d_ff=128, T=T)
+        return lib.moe_forward_train(ctypes.byref(cc), x, f, None, None, None, f, f, f, f, ws_bytes, y, None)
+    assert fwd_train(x=None) == 1
+    assert fwd_train(y=odd) == 1
+    assert fwd_train(ws_bytes=need - 1) == 3
+    assert fwd_train(T=0, x=None, y=None, ws_bytes=0) == 0
