@@ -1,4 +1,5 @@
-// router.cuh -- the gate: fp32 router GEMM with fused softmax and top-k.
+// router.cuh -- the gate: the fp32 router GEMM on the CUDA cores, and the
+// per-token softmax / top-k kernel that finishes every router form.
 //
 // DeepSeekMoE translation (gitcode.csdn.net), section 3.2, eqs (10)-(11):
 //   s_t = Softmax_i(u_t^T e_i) over the routed experts, g_{i,t} = s_{i,t} on

@@ -39,8 +39,9 @@
 //               logits row [T][NP] in fp32 to the router scratch.
 // The softmax, keys, top-k and gates of every token are then computed by
 // router_finish_kernel (router.cuh), launched as this kernel's programmatic
-// dependent: one warp per token at full occupancy, where a once-per-CTA tail
-// here ran with a cold instruction cache and one or two warps per scheduler.
+// dependent: NP / 8 lanes per token at full occupancy, where a once-per-CTA
+// tail here ran with a cold instruction cache and one or two warps per
+// scheduler.
 #pragma once
 
 #include "common.cuh"
